@@ -188,6 +188,28 @@ def _t54(wl: Workload, f: int):
     return ref, np.zeros_like(ref)
 
 
+def _parity_stress(wl: Workload, f: int):
+    # Past 2^55 units with codeword 65535, then a seeded mix whose squares
+    # tie at the last place 8 (p = 2 mod 4 below 4096), move the parity of
+    # S / 8 (p in [8192, 11585), squares that are odd multiples of 8 about
+    # half the time) or round down (odd p below 4096). dis: the same recipe
+    # with another draw, past 2^54 only.
+    g = _rng(wl.seed, f)
+    n = wl.width * wl.height
+    planes = []
+    for fill in (8388864 + 4096, 4194432 + 64 * 4096):
+        plane = np.zeros(n, dtype=np.uint16)
+        plane[:fill] = 65535
+        m = n - fill
+        kind = g.integers(0, 3, size=m)
+        tie = 4 * g.integers(0, 1024, size=m) + 2
+        flip = g.integers(8192, 11585, size=m)
+        down = 2 * g.integers(0, 2048, size=m) + 1
+        plane[fill:] = np.where(kind == 0, tie, np.where(kind == 1, flip, down))
+        planes.append(plane.reshape(wl.height, wl.width))
+    return planes[0], planes[1]
+
+
 _RECIPES: dict = {
     "c1": _c1,
     "c2": _c2,
@@ -198,6 +220,7 @@ _RECIPES: dict = {
     "past53": _uniform_pair(40000, 65535, 40000, 65535),
     "past55": _uniform_pair(60000, 65535, 60000, 65535),
     "t54": _t54,
+    "parity": _parity_stress,
 }
 
 WORKLOADS = {
@@ -212,6 +235,8 @@ WORKLOADS = {
     "T1": Workload("T1", 2560, 1440, 16, 1, 6, "past53"),
     "T2": Workload("T2", 4096, 2560, 16, 1, 7, "past55"),
     "T3": Workload("T3", 3840, 2160, 16, 1, 0, "t54"),
+    # Parity stress: binade 55 with ties and parity changes in every row.
+    "T4": Workload("T4", 4096, 2560, 16, 2, 8, "parity"),
 }
 
 

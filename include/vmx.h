@@ -1,0 +1,151 @@
+/*
+ * vmx.h -- C ABI of libvmx: bit-exact float_moment and float_psnr of 8- to
+ * 16-bit luma frame pairs on a CUDA GPU (sm_103a).
+ *
+ * What is computed (the CPU extractors the results must equal bit for bit):
+ *
+ *   Samples p are unsigned codewords; scaler = 2^(bpc - 8); the CPU puts every
+ *   sample on the 8-bit scale as the binary32 value p / scaler.
+ *
+ *   float_moment (ADR-1497 "Context"; Research-2081 "Selected restoration"):
+ *     first moment  = mean of p / scaler, raster order, double accumulator;
+ *     second moment = one binary32 square per pixel, fl32((p/scaler)^2), added
+ *                     into a double in raster order, divided by the pixel
+ *                     count. Past 2^53 units the CPU's running double rounds
+ *                     on every add; the library reproduces that rounding
+ *                     value for value (ADR-1497 "Decision").
+ *   float_psnr (ADR-1499 "Context" and "Decision"):
+ *     each row's sum of binary32 squared sample differences (exact, below
+ *     2^47 units), the rows added into one double in row order, divided by
+ *     the pixel count: the MSE on the 8-bit scale.
+ *
+ *   "Units" are 1/scaler^2: every float square is an integer below 2^32 in
+ *   them, and the library forms every sum as an integer in these units.
+ *
+ * Layout of the inputs: frame f of a batch starts at base + f * height *
+ * stride_bytes; row i of a frame at + i * stride_bytes. bpc == 8 means uint8
+ * samples, 9..16 means uint16 samples in host (little-endian) byte order.
+ * Samples above 2^bpc - 1 are used as they are (the CPU does not clamp).
+ *
+ * Limits: 1 <= width <= 32768 (a row has at most 2^15 terms, ADR-1499
+ * "Decision" point 1), height >= 1, width * height <= 2^25, nframes >= 1,
+ * stride_bytes >= width * bytes per sample.
+ *
+ * Streams: every call enqueues its work on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and returns without waiting, except where a
+ * function says it synchronises. Calls that share one workspace must not run
+ * concurrently.
+ *
+ * Errors: every int-returning function returns VMX_OK (0) or a negative code.
+ * On an argument error nothing is launched and no output is written.
+ */
+#ifndef VMX_H
+#define VMX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VMX_OK 0
+#define VMX_EINVAL (-1)    /* bad argument: pointer, size, bpc, stride, workspace size */
+#define VMX_ENOMEM (-2)    /* the library could not allocate device memory */
+#define VMX_ECUDA (-3)     /* a CUDA call failed; vmx_strerror() names it */
+#define VMX_ETIMEOUT (-4)  /* a bounded device wait gave up; outputs are not valid */
+
+#define VMX_FEATURE_MOMENT 1 /* float_moment: 4 doubles per frame */
+#define VMX_FEATURE_PSNR 2   /* float_psnr: row sums and the MSE per frame */
+
+/* Bytes of device workspace a call needs for this shape and these features
+ * (VMX_FEATURE_* bits). Returns 0 for arguments the calls would reject. */
+size_t vmx_workspace_bytes(int width, int height, int bpc, int nframes, int features);
+
+/*
+ * float_moment of nframes frame pairs (ADR-1497; Research-2081).
+ *   ref, dis      device pointers to the first frame of each batch.
+ *   moments       device, [nframes][4] doubles: ref first moment, dis first
+ *                 moment, ref second moment, dis second moment.
+ *   s2_rows       device or NULL, [nframes][2][height] uint64: each row's
+ *                 exact sum of the binary32 squares in units (ref rows, then
+ *                 dis rows).
+ *   workspace     device memory of at least vmx_workspace_bytes(...,
+ *                 VMX_FEATURE_MOMENT) bytes, caller-owned; or NULL, in which
+ *                 case the call allocates and frees it on `stream`.
+ * Asynchronous on `stream`. A bounded device wait that gives up is reported
+ * by vmx_workspace_status() on the same workspace.
+ */
+int vmx_moment_frames(const void *ref, const void *dis, int width, int height,
+                      int64_t stride_bytes, int bpc, int nframes, double *moments,
+                      uint64_t *s2_rows, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/*
+ * float_psnr of nframes frame pairs (ADR-1499).
+ *   rows   device, [nframes][height] uint64: each row's exact sum of the
+ *          binary32 squared differences in units of 1/scaler^2.
+ *   mse    device, [nframes] doubles: the CPU's row-order noise / pixels.
+ * The PSNR itself is a host function of the MSE: vmx_psnr_db().
+ * Workspace, stream and errors as vmx_moment_frames().
+ */
+int vmx_float_psnr_frames(const void *ref, const void *dis, int width, int height,
+                          int64_t stride_bytes, int bpc, int nframes, uint64_t *rows,
+                          double *mse, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/*
+ * Both features in one read of both planes. Same arguments as the two calls
+ * above; the workspace is vmx_workspace_bytes(..., VMX_FEATURE_MOMENT |
+ * VMX_FEATURE_PSNR). Outputs as above; s2_rows may be NULL.
+ */
+int vmx_moment_psnr_frames(const void *ref, const void *dis, int width, int height,
+                           int64_t stride_bytes, int bpc, int nframes, double *moments,
+                           uint64_t *s2_rows, uint64_t *psnr_rows, double *mse,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Status of the last call that used `workspace`: VMX_OK, or VMX_ETIMEOUT if a
+ * bounded device wait gave up. Synchronises `stream`.
+ */
+int vmx_workspace_status(const void *workspace, void *stream);
+
+/*
+ * PSNR in dB from the MSE on the 8-bit scale, on the host:
+ * 10 * log10(peak^2 / max(mse, 1e-10)) with peak = (2^bpc - 1) / 2^(bpc - 8),
+ * capped at psnr_max when psnr_max > 0. The pages give no formula; this is
+ * the reading the library takes. Host arrays of n doubles.
+ */
+int vmx_psnr_db(const double *mse, int n, int bpc, double psnr_max, double *psnr);
+
+/*
+ * Host-memory entry point: frames in host memory (pinned recommended),
+ * results in host memory. Copies chunks of `chunk_frames` frames to the
+ * device on `stream` while the previous chunk computes on a second stream
+ * the library creates, then copies the results back. Synchronises before it
+ * returns. features: VMX_FEATURE_* bits; outputs of a feature not asked for
+ * may be NULL, as may s2_rows and psnr (psnr needs VMX_FEATURE_PSNR).
+ *   workspace  device memory of vmx_host_workspace_bytes(...) bytes, or NULL
+ *              (then allocated and freed by the call).
+ */
+size_t vmx_host_workspace_bytes(int width, int height, int bpc, int chunk_frames,
+                                int features);
+int vmx_frames_host(const void *ref, const void *dis, int width, int height,
+                    int64_t stride_bytes, int bpc, int nframes, int features,
+                    double *moments, uint64_t *s2_rows, uint64_t *psnr_rows, double *mse,
+                    double *psnr, double psnr_max, int chunk_frames, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/* Name of a status code (and the last CUDA error for VMX_ECUDA). */
+const char *vmx_strerror(int status);
+
+/* Launches of the library's own kernels since load (a counter). */
+uint64_t vmx_kernel_launches(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int vmx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VMX_H */

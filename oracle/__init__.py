@@ -52,6 +52,10 @@ def _bind(path: str) -> ctypes.CDLL:
                               ctypes.POINTER(ctypes.c_uint64))
     lib.vmx_oracle_moment.argtypes = [vp, vp, i32, i32, i64, i32, dp, u64p]
     lib.vmx_oracle_moment.restype = None
+    lib.vmx_oracle_moment_acc.argtypes = [vp, vp, i32, i32, i64, i32, dp]
+    lib.vmx_oracle_moment_acc.restype = None
+    lib.vmx_oracle_psnr_noise.argtypes = [vp, vp, i32, i32, i64, i32, u64p]
+    lib.vmx_oracle_psnr_noise.restype = ctypes.c_double
     lib.vmx_oracle_psnr.argtypes = [vp, vp, i32, i32, i64, i32, u64p, dp]
     lib.vmx_oracle_psnr.restype = None
     lib.vmx_oracle_psnr_db.argtypes = [ctypes.c_double, i32, ctypes.c_double]
@@ -95,6 +99,42 @@ def moment(ref: np.ndarray, dis: np.ndarray, bpc: int, rows: bool = False,
                           out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                           r.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)) if rows else None)
     return (out, r) if rows else out
+
+
+def moment_sums(ref: np.ndarray, dis: np.ndarray, bpc: int, mutation: int = 0,
+                width: Optional[int] = None) -> Tuple[int, int, int, int]:
+    """The CPU's four accumulators after the last pixel, as exact integers in
+    units: (sum p / scaler in 1/scaler, same for dis, second-moment sums of
+    ref and dis in 1/scaler^2)."""
+    lib = load(mutation)
+    pr, pd, w, h, s = _plane_args(ref, dis, width)
+    acc = np.zeros(4, dtype=np.float64)
+    lib.vmx_oracle_moment_acc(pr, pd, w, h, s, bpc,
+                              acc.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    k = bpc - 8
+    return (_units(acc[0], k), _units(acc[1], k), _units(acc[2], 2 * k), _units(acc[3], 2 * k))
+
+
+def psnr_noise_sum(ref: np.ndarray, dis: np.ndarray, bpc: int, mutation: int = 0,
+                   width: Optional[int] = None) -> int:
+    """The CPU's row-order noise accumulator as an exact integer in units."""
+    lib = load(mutation)
+    pr, pd, w, h, s = _plane_args(ref, dis, width)
+    noise = lib.vmx_oracle_psnr_noise(pr, pd, w, h, s, bpc, None)
+    return _units(noise, 2 * (bpc - 8))
+
+
+def _units(x: float, shift: int) -> int:
+    """A double holding a multiple of 2^-shift, as that integer multiple."""
+    import math
+    if x == 0.0:
+        return 0
+    m, e = math.frexp(x)
+    mant = int(m * 2**53)  # exact: 53 significant bits
+    sh = e - 53 + shift
+    v = mant << sh if sh >= 0 else mant >> -sh
+    assert sh >= 0 or mant & ((1 << -sh) - 1) == 0, "not a multiple of the unit"
+    return v
 
 
 def psnr(ref: np.ndarray, dis: np.ndarray, bpc: int, mutation: int = 0,

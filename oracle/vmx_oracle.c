@@ -86,7 +86,7 @@ static double pixel_count(int width, int height)
 
 /* First moment: the mean of the normalised samples (ADR-1212 normalisation
  * as recalled in Research-2081 "Selected restoration"), raster order. */
-static double first_moment(const void *plane, int w, int h, int64_t stride, int bpc)
+static double first_moment_acc(const void *plane, int w, int h, int64_t stride, int bpc)
 {
     const float scaler = scaler_of(bpc);
 #if ORACLE_MUTATION == 9
@@ -101,13 +101,13 @@ static double first_moment(const void *plane, int w, int h, int64_t stride, int 
             acc += (double)f;
         }
     }
-    return (double)acc / pixel_count(w, h);
+    return (double)acc;
 }
 
 /* Second moment, moment.c::compute_2nd_moment() as ADR-1497 "Context"
  * states it: one binary32 square per pixel added into a double in raster
  * order, then divided by the pixel count. */
-static double second_moment(const void *plane, int w, int h, int64_t stride, int bpc)
+static double second_moment_acc(const void *plane, int w, int h, int64_t stride, int bpc)
 {
     const float scaler = scaler_of(bpc);
 #if ORACLE_MUTATION == 2
@@ -134,7 +134,7 @@ static double second_moment(const void *plane, int w, int h, int64_t stride, int
 #endif
         }
     }
-    return (double)acc / pixel_count(w, h);
+    return (double)acc;
 }
 
 /* Each row's sum of binary32 squares in units of 1/scaler^2. A row has at
@@ -161,19 +161,33 @@ static void second_moment_rows(const void *plane, int w, int h, int64_t stride, 
     }
 }
 
-void vmx_oracle_moment(const void *ref, const void *dis, int width, int height,
-                       int64_t stride_bytes, int bpc, double out[4], uint64_t *s2_rows)
+void vmx_oracle_moment_acc(const void *ref, const void *dis, int width, int height,
+                           int64_t stride_bytes, int bpc, double acc[4])
 {
 #if ORACLE_MUTATION == 11
     const void *a = dis, *b = ref;
 #else
     const void *a = ref, *b = dis;
 #endif
-    out[0] = first_moment(a, width, height, stride_bytes, bpc);
-    out[1] = first_moment(b, width, height, stride_bytes, bpc);
-    out[2] = second_moment(a, width, height, stride_bytes, bpc);
-    out[3] = second_moment(b, width, height, stride_bytes, bpc);
+    acc[0] = first_moment_acc(a, width, height, stride_bytes, bpc);
+    acc[1] = first_moment_acc(b, width, height, stride_bytes, bpc);
+    acc[2] = second_moment_acc(a, width, height, stride_bytes, bpc);
+    acc[3] = second_moment_acc(b, width, height, stride_bytes, bpc);
+}
+
+void vmx_oracle_moment(const void *ref, const void *dis, int width, int height,
+                       int64_t stride_bytes, int bpc, double out[4], uint64_t *s2_rows)
+{
+    double acc[4];
+    vmx_oracle_moment_acc(ref, dis, width, height, stride_bytes, bpc, acc);
+    for (int i = 0; i < 4; ++i)
+        out[i] = acc[i] / pixel_count(width, height);
     if (s2_rows) {
+#if ORACLE_MUTATION == 11
+        const void *a = dis, *b = ref;
+#else
+        const void *a = ref, *b = dis;
+#endif
         second_moment_rows(a, width, height, stride_bytes, bpc, s2_rows);
         second_moment_rows(b, width, height, stride_bytes, bpc, s2_rows + height);
     }
@@ -184,8 +198,8 @@ void vmx_oracle_moment(const void *ref, const void *dis, int width, int height,
  * (noise_line()), the rows into one double in row order, then the CPU's
  * divisions (by scaler^2 through the normalisation, and by the pixel
  * count). */
-void vmx_oracle_psnr(const void *ref, const void *dis, int width, int height,
-                     int64_t stride_bytes, int bpc, uint64_t *rows, double *mse)
+double vmx_oracle_psnr_noise(const void *ref, const void *dis, int width, int height,
+                             int64_t stride_bytes, int bpc, uint64_t *rows)
 {
     const float scaler = scaler_of(bpc);
     const int k2 = 2 * (bpc - 8);
@@ -223,6 +237,13 @@ void vmx_oracle_psnr(const void *ref, const void *dis, int width, int height,
 #if ORACLE_MUTATION == 4
     noise = ldexp((double)exact_total, -k2);
 #endif
+    return noise;
+}
+
+void vmx_oracle_psnr(const void *ref, const void *dis, int width, int height,
+                     int64_t stride_bytes, int bpc, uint64_t *rows, double *mse)
+{
+    const double noise = vmx_oracle_psnr_noise(ref, dis, width, height, stride_bytes, bpc, rows);
 #if ORACLE_MUTATION == 13
     *mse = (double)((float)noise / (float)pixel_count(width, height));
 #else

@@ -25,6 +25,16 @@ void vmx_oracle_moment(const void *ref, const void *dis, int width, int height,
                        int64_t stride_bytes, int bpc, double out[4],
                        uint64_t *s2_rows);
 
+/* The four accumulators of vmx_oracle_moment() before the division by the
+ * pixel count: the CPU's running doubles (true scale) after the last pixel. */
+void vmx_oracle_moment_acc(const void *ref, const void *dis, int width, int height,
+                           int64_t stride_bytes, int bpc, double acc[4]);
+
+/* The psnr noise accumulator before the division by the pixel count (the
+ * CPU's row-order double, true scale); rows as vmx_oracle_psnr(). */
+double vmx_oracle_psnr_noise(const void *ref, const void *dis, int width, int height,
+                             int64_t stride_bytes, int bpc, uint64_t *rows);
+
 /* float_psnr of one frame pair: rows[height] receives each row's sum of the
  * float squared differences in units of 1/scaler^2; *mse the frame noise
  * divided by the pixel count. rows may be NULL. */

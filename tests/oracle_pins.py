@@ -55,6 +55,8 @@ def pin_tiny_bruteforce(mutation=0, seeds=range(24)):
         want, want_rows = moment_model(ref, dis, bpc)
         got, got_rows = oracle.moment(ref, dis, bpc, rows=True, mutation=mutation)
         _eq(got, want, f"moments seed {s} bpc {bpc} {w}x{h}")
+        sums = oracle.moment_sums(ref, dis, bpc, mutation=mutation)
+        assert sums[2:] == tuple(ordered_sum(squares_units(x).ravel()) for x in (ref, dis))
         assert np.array_equal(got_rows, want_rows), f"s2 rows seed {s}"
         prow, pmse = psnr_model(ref, dis, bpc)
         grow, gmse = oracle.psnr(ref, dis, bpc, mutation=mutation)
@@ -107,10 +109,18 @@ def pin_past_2_53_bruteforce(mutation=0):
     """A 2560x1440 16-bit frame past 2^53 units (ADR-1497 "Context"): the
     second moments equal the raster-order integer recurrence; the first
     moments the exact quotient."""
-    ref, dis = _t1()
-    got = oracle.moment(ref, dis, 16, mutation=mutation)
-    want, _ = moment_model(ref, dis, 16)
-    _eq(got, want, "moments of the 2560x1440 frame past 2^53")
+    for ref, dis in (_t1(), _parity()):
+        got = oracle.moment(ref, dis, 16, mutation=mutation)
+        want, _ = moment_model(ref, dis, 16)
+        _eq(got, want, "moments of a frame past 2^53")
+        sums = oracle.moment_sums(ref, dis, 16, mutation=mutation)
+        assert sums[2:] == tuple(ordered_sum(squares_units(x).ravel()) for x in (ref, dis)), \
+            "second-moment sums of a frame past 2^53"
+
+
+@lru_cache(maxsize=None)
+def _parity():
+    return synth.WORKLOADS["T4"].frame(0)
 
 
 @lru_cache(maxsize=None)
@@ -127,6 +137,7 @@ def pin_psnr_row_order(mutation=0):
     grow, gmse = oracle.psnr(ref, dis, 16, mutation=mutation)
     assert np.array_equal(grow, prow), "psnr rows of the half-range frame"
     _eq(gmse, pmse, "mse of the half-range frame")
+    assert oracle.psnr_noise_sum(ref, dis, 16, mutation=mutation) == ordered_sum(prow)
 
 
 def pin_constructed_frames(mutation=0):
@@ -143,6 +154,8 @@ def pin_constructed_frames(mutation=0):
         assert int(t.sum(dtype=np.uint64)) == exact, name
         got = oracle.moment(ref, dis, 16, mutation=mutation)
         _eq(got[2], scaled_mean(cpu, 16, n), f"second moment {name}")
+        assert oracle.moment_sums(ref, dis, 16, mutation=mutation)[2] == cpu, name
+        assert oracle.psnr_noise_sum(ref, dis, 16, mutation=mutation) == cpu, name
         _eq(got[3], 0.0, f"dis second moment {name}")
         rows, mse = oracle.psnr(ref, dis, 16, mutation=mutation)
         assert int(rows.sum(dtype=np.uint64)) == exact, name
