@@ -81,7 +81,7 @@ def build_lib(force: bool = False, verbose: bool = False) -> str:
         list(ex.map(_run, cmds))
     tmp = LIB + f".tmp{os.getpid()}"
     _run([NVCC, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-          "-Xlinker", f"-rpath,{CUDA_HOME}/lib64", "-lcuda"])
+          "-Xlinker", f"-rpath,{CUDA_HOME}/lib64"])
     os.replace(tmp, LIB)
     if verbose:
         print("built", LIB)

@@ -112,19 +112,84 @@ VMX_HD uint64_t apply(const Run &r, uint64_t s, int sh)
     return s + r.inc[(s >> sh) & 1ull];
 }
 
-// The binary32 square of a codeword p < 2^16, as the exact integer it is
-// (p^2 rounded to 24 significant bits): the CPU's term in units.
-VMX_HD uint32_t term_of_sample(uint32_t p)
+VMX_HD float as_float(uint32_t u)
 {
 #if defined(__CUDA_ARCH__)
-    const float f = __uint2float_rn(p);
-    return __float2uint_rn(__fmul_rn(f, f));
+    return __uint_as_float(u);
 #else
-    const float f = (float)p;
-    volatile float sq = f * f;
-    return (uint32_t)sq;
+    float f;
+    __builtin_memcpy(&f, &u, sizeof f);
+    return f;
 #endif
 }
+
+VMX_HD uint32_t as_uint(float f)
+{
+#if defined(__CUDA_ARCH__)
+    return __float_as_uint(f);
+#else
+    uint32_t u;
+    __builtin_memcpy(&u, &f, sizeof u);
+    return u;
+#endif
+}
+
+// Binary32 add, multiply and fused multiply-add, each rounded once to
+// nearest even, never contracted or reassociated.
+VMX_HD float f32_add(float a, float b)
+{
+#if defined(__CUDA_ARCH__)
+    return __fadd_rn(a, b);
+#else
+    volatile float r = a + b;
+    return r;
+#endif
+}
+
+VMX_HD float f32_mul(float a, float b)
+{
+#if defined(__CUDA_ARCH__)
+    return __fmul_rn(a, b);
+#else
+    volatile float r = a * b;
+    return r;
+#endif
+}
+
+VMX_HD float f32_fma(float a, float b, float c)
+{
+#if defined(__CUDA_ARCH__)
+    return __fmaf_rn(a, b, c);
+#else
+    return __builtin_fmaf(a, b, c);
+#endif
+}
+
+// Small integers to and from binary32 without a conversion instruction:
+// 2^23 + v has v in its low mantissa bits for 0 <= v < 2^23, and
+// 1.5 * 2^23 + i has i + 2^22 there for |i| < 2^22.
+constexpr uint32_t kMagicU = 0x4B000000u;  // 2^23
+constexpr uint32_t kMagicI = 0x4B400000u;  // 1.5 * 2^23
+VMX_HD float small_u_to_f(uint32_t v) { return f32_add(as_float(v | kMagicU), -8388608.0f); }
+VMX_HD int32_t small_f_to_i(float x)
+{
+    return (int32_t)(as_uint(f32_add(x, 12582912.0f)) - kMagicI);
+}
+// Inverse of small_u_to_f for an integral 0 <= x < 2^23.
+VMX_HD uint32_t small_f_to_u(float x) { return as_uint(f32_add(x, 8388608.0f)) - kMagicU; }
+
+// The binary32 square of a codeword p < 2^16 given f = (float)p, as the
+// exact integer it is (p^2 rounded to 24 significant bits): p^2 minus the
+// product's rounding error, which the fused multiply-add gives exactly.
+VMX_HD uint32_t term_from_float(uint32_t p, float f)
+{
+    const float tf = f32_mul(f, f);
+    const float ef = f32_fma(f, f, -tf);  // p^2 - tf, an integer in [-128, 128]
+    return p * p - (uint32_t)small_f_to_i(ef);
+}
+
+// The CPU's term in units for a codeword p < 2^16.
+VMX_HD uint32_t term_of_sample(uint32_t p) { return term_from_float(p, small_u_to_f(p)); }
 
 // The binary32 square of a difference of codewords, |d| < 2^16.
 VMX_HD uint32_t term_of_diff(uint32_t a, uint32_t b)
@@ -185,9 +250,9 @@ VMX_HD Run lane_to_run(const LaneRun &r, uint64_t exact)
 // higher; eight adds of v < 2u never leave the binade.
 VMX_HD LaneRun lane_run_fp(const uint32_t *t, int n, int sh)
 {
-    const float uf = (float)(1u << sh);
-    const float f0e = 12582912.0f * uf;  // 1.5 * 2^23 * u
-    const float f0o = f0e + uf;
+    const float uf = as_float((uint32_t)(127 + sh) << 23);  // 2^sh
+    const float f0e = f32_mul(12582912.0f, uf);              // 1.5 * 2^23 * u
+    const float f0o = f32_add(f0e, uf);
     float fe = f0e, fo = f0o;
     uint32_t tlo = 0, vsum = 0;
     const uint32_t vmask = (2u << sh) - 1u;
@@ -195,21 +260,14 @@ VMX_HD LaneRun lane_run_fp(const uint32_t *t, int n, int sh)
         const uint32_t v = t[i] & vmask;
         tlo += t[i];
         vsum += v;
-        const float vf = (float)v;
-#if defined(__CUDA_ARCH__)
-        fe = __fadd_rn(fe, vf);
-        fo = __fadd_rn(fo, vf);
-#else
-        volatile float a = fe + vf;
-        volatile float b = fo + vf;
-        fe = a;
-        fo = b;
-#endif
+        const float vf = small_u_to_f(v);
+        fe = f32_add(fe, vf);
+        fo = f32_add(fo, vf);
     }
     LaneRun r;
     r.tlo = tlo;
-    r.d[0] = (int32_t)(fe - f0e) - (int32_t)vsum;
-    r.d[1] = (int32_t)(fo - f0o) - (int32_t)vsum;
+    r.d[0] = small_f_to_i(f32_add(fe, -f0e)) - (int32_t)vsum;
+    r.d[1] = small_f_to_i(f32_add(fo, -f0o)) - (int32_t)vsum;
     if (VMX_MUT(2)) r.d[1] = r.d[0];  // parity ignored
     return r;
 }

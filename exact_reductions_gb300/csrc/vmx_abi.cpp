@@ -1,0 +1,444 @@
+// vmx_abi.cpp -- the C ABI of libvmx: argument checks, the workspace layout,
+// the launch of the frame kernel, and the host-memory pipeline.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "vmx.h"
+#include "vmx_internal.h"
+
+namespace vmx {
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_last_cuda[160] = "";
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int cuda_fail(cudaError_t e)
+{
+    std::snprintf(g_last_cuda, sizeof g_last_cuda, "%s: %s", cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return e == cudaErrorMemoryAllocation ? VMX_ENOMEM : VMX_ECUDA;
+}
+
+// Host-side fault injection for tests: VMX_TEST_FAIL_AT=alloc|launch|status
+// makes that stage fail without touching the GPU.
+bool fail_at(const char *stage)
+{
+    const char *v = std::getenv("VMX_TEST_FAIL_AT");
+    return v && std::strcmp(v, stage) == 0;
+}
+
+int bytes_per_sample(int bpc) { return bpc == 8 ? 1 : 2; }
+
+}  // namespace
+
+bool make_layout(int width, int height, int bpc, int frames, int features, Layout *L)
+{
+    if (width < 1 || width > 32768 || height < 1 || frames < 1 || bpc < 8 || bpc > 16)
+        return false;
+    if ((int64_t)width * height > (int64_t)1 << 25) return false;
+    if (features < 1 || features > 3) return false;
+    const int rows_per_warp = std::max(1, (2048 + width - 1) / width);
+    const int rpt = std::min(kMaxRowsPerTile, kWarps * rows_per_warp);
+    const int tpf = (height + rpt - 1) / rpt;
+    if ((int64_t)frames * tpf >= (int64_t)INT_MAX / 2) return false;
+    const size_t F = (size_t)frames, T = (size_t)tpf, H = (size_t)height;
+    L->width = width;
+    L->height = height;
+    L->frames = frames;
+    L->bpc = bpc;
+    L->features = features;
+    L->rows_per_tile = rpt;
+    L->tiles_per_frame = tpf;
+    L->ordered = bpc > 8 && (int64_t)width * height > ((int64_t)1 << 21) &&
+                 (features & VMX_FEATURE_MOMENT);
+    size_t off = 0;
+    L->off_ctrl = off;
+    L->ctrl_bytes = (kCtrlWords + F + F * T) * sizeof(uint32_t);
+    off = align256(off + L->ctrl_bytes);
+    L->off_tile_agg = off;
+    off = align256(off + F * T * 2 * sizeof(uint64_t));
+    L->off_tile_inc = off;
+    off = align256(off + F * T * 2 * sizeof(uint64_t));
+    L->off_tile_s1 = off;
+    off = align256(off + F * T * 2 * sizeof(uint64_t));
+    L->off_s2_rows = off;
+    if (features & VMX_FEATURE_MOMENT) off = align256(off + F * 2 * H * sizeof(uint64_t));
+    L->off_psnr_rows = off;
+    L->off_rec = off;
+    if (L->ordered) off = align256(off + F * 2 * H * sizeof(RowRec));
+    L->total = off;
+    return true;
+}
+
+namespace {
+
+struct Outputs {
+    double *moments;
+    uint64_t *s2_rows, *s2_sums, *psnr_rows;
+    double *mse;
+    uint64_t *noise_sums;
+};
+
+// status: where a bounded wait that gave up is recorded; NULL for the
+// workspace's own status word (cleared with the other control words).
+int run_frames(const void *ref, const void *dis, int width, int height, int64_t stride,
+               int bpc, int nframes, int features, const Outputs &o, void *workspace,
+               size_t workspace_bytes, cudaStream_t stream, uint32_t *status_word = nullptr)
+{
+    Layout L;
+    if (!ref || !dis || !make_layout(width, height, bpc, nframes, features, &L)) return VMX_EINVAL;
+    if (stride < (int64_t)width * bytes_per_sample(bpc)) return VMX_EINVAL;
+    if ((features & VMX_FEATURE_MOMENT) && !o.moments) return VMX_EINVAL;
+    if ((features & VMX_FEATURE_PSNR) && (!o.psnr_rows || !o.mse)) return VMX_EINVAL;
+    if (bpc > 8 && ((uintptr_t)ref % 2 || (uintptr_t)dis % 2 || stride % 2)) return VMX_EINVAL;
+    const bool own = workspace == nullptr;
+    if (!own && (workspace_bytes < L.total || (uintptr_t)workspace % 256)) return VMX_EINVAL;
+    if (fail_at("alloc")) return VMX_ENOMEM;
+    if (fail_at("launch")) {
+        std::snprintf(g_last_cuda, sizeof g_last_cuda, "injected launch failure");
+        return VMX_ECUDA;
+    }
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    cudaError_t err;
+    if (own) {
+        void *p = nullptr;
+        err = cudaMallocAsync(&p, L.total, stream);
+        if (err != cudaSuccess) return cuda_fail(err);
+        ws = static_cast<unsigned char *>(p);
+    }
+    Params p;
+    p.ref = static_cast<const unsigned char *>(ref);
+    p.dis = static_cast<const unsigned char *>(dis);
+    p.stride = stride;
+    p.pitch = stride * height;
+    p.width = width;
+    p.height = height;
+    p.frames = nframes;
+    p.k = bpc - 8;
+    p.rows_per_tile = L.rows_per_tile;
+    p.tiles_per_frame = L.tiles_per_frame;
+    p.ctrl = reinterpret_cast<uint32_t *>(ws + L.off_ctrl);
+    p.done = p.ctrl + kCtrlWords;
+    p.flags = p.done + nframes;
+    p.status = status_word ? status_word : p.ctrl + kCtrlStatus;
+    p.tile_agg = reinterpret_cast<uint64_t *>(ws + L.off_tile_agg);
+    p.tile_inc = reinterpret_cast<uint64_t *>(ws + L.off_tile_inc);
+    p.tile_s1 = reinterpret_cast<uint64_t *>(ws + L.off_tile_s1);
+    p.s2_rows = o.s2_rows ? o.s2_rows : reinterpret_cast<uint64_t *>(ws + L.off_s2_rows);
+    p.psnr_rows = o.psnr_rows;
+    p.rec = reinterpret_cast<RowRec *>(ws + L.off_rec);
+    p.moments = o.moments;
+    p.mse = o.mse;
+    p.s2_sums = o.s2_sums;
+    p.noise_sums = o.noise_sums;
+    p.spin_limit = kSpinLimit;
+    const bool vec = (uintptr_t)ref % 16 == 0 && (uintptr_t)dis % 16 == 0 && stride % 16 == 0;
+    err = cudaMemsetAsync(ws + L.off_ctrl, 0, L.ctrl_bytes, stream);
+    if (err == cudaSuccess) {
+        err = launch_frames(p, L, features, vec, stream);
+        if (err == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    if (!own) return err == cudaSuccess ? VMX_OK : cuda_fail(err);
+    int status = VMX_OK;
+    uint32_t dev_status = 0;
+    if (err == cudaSuccess)
+        err = cudaMemcpyAsync(&dev_status, p.ctrl + kCtrlStatus, sizeof dev_status,
+                              cudaMemcpyDeviceToHost, stream);
+    const cudaError_t ferr = cudaFreeAsync(ws, stream);
+    if (err == cudaSuccess) err = ferr;
+    if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+    if (err != cudaSuccess) status = cuda_fail(err);
+    else if (dev_status) status = VMX_ETIMEOUT;
+    return status;
+}
+
+}  // namespace
+}  // namespace vmx
+
+using namespace vmx;
+
+extern "C" {
+
+int vmx_version(void) { return 10000; }
+
+uint64_t vmx_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *vmx_strerror(int status)
+{
+    switch (status) {
+    case VMX_OK: return "ok";
+    case VMX_EINVAL: return "invalid argument";
+    case VMX_ENOMEM: return "out of device memory";
+    case VMX_ECUDA: return g_last_cuda[0] ? g_last_cuda : "CUDA error";
+    case VMX_ETIMEOUT: return "a bounded device wait gave up";
+    default: return "unknown status";
+    }
+}
+
+size_t vmx_workspace_bytes(int width, int height, int bpc, int nframes, int features)
+{
+    Layout L;
+    if (!make_layout(width, height, bpc, nframes, features, &L)) return 0;
+    return L.total;
+}
+
+int vmx_moment_frames(const void *ref, const void *dis, int width, int height,
+                      int64_t stride_bytes, int bpc, int nframes, double *moments,
+                      uint64_t *s2_rows, uint64_t *s2_sums, void *workspace,
+                      size_t workspace_bytes, void *stream)
+{
+    const Outputs o{moments, s2_rows, s2_sums, nullptr, nullptr, nullptr};
+    return run_frames(ref, dis, width, height, stride_bytes, bpc, nframes, VMX_FEATURE_MOMENT, o,
+                      workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int vmx_float_psnr_frames(const void *ref, const void *dis, int width, int height,
+                          int64_t stride_bytes, int bpc, int nframes, uint64_t *rows,
+                          double *mse, uint64_t *noise_sums, void *workspace,
+                          size_t workspace_bytes, void *stream)
+{
+    const Outputs o{nullptr, nullptr, nullptr, rows, mse, noise_sums};
+    return run_frames(ref, dis, width, height, stride_bytes, bpc, nframes, VMX_FEATURE_PSNR, o,
+                      workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int vmx_moment_psnr_frames(const void *ref, const void *dis, int width, int height,
+                           int64_t stride_bytes, int bpc, int nframes, double *moments,
+                           uint64_t *s2_rows, uint64_t *s2_sums, uint64_t *psnr_rows,
+                           double *mse, uint64_t *noise_sums, void *workspace,
+                           size_t workspace_bytes, void *stream)
+{
+    const Outputs o{moments, s2_rows, s2_sums, psnr_rows, mse, noise_sums};
+    return run_frames(ref, dis, width, height, stride_bytes, bpc, nframes,
+                      VMX_FEATURE_MOMENT | VMX_FEATURE_PSNR, o, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int vmx_workspace_status(const void *workspace, void *stream)
+{
+    if (!workspace) return VMX_EINVAL;
+    if (fail_at("status")) return VMX_ETIMEOUT;
+    uint32_t v = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint32_t *ctrl = reinterpret_cast<const uint32_t *>(workspace);
+    cudaError_t err = cudaMemcpyAsync(&v, ctrl + kCtrlStatus, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+    if (err != cudaSuccess) return cuda_fail(err);
+    return v ? VMX_ETIMEOUT : VMX_OK;
+}
+
+int vmx_workspace_stats(const void *workspace, void *stream, uint64_t *out4)
+{
+    if (!workspace || !out4) return VMX_EINVAL;
+    uint32_t v[4] = {0, 0, 0, 0};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint32_t *ctrl = reinterpret_cast<const uint32_t *>(workspace);
+    cudaError_t err =
+        cudaMemcpyAsync(v, ctrl + kCtrlRowsExact, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+    if (err != cudaSuccess) return cuda_fail(err);
+    for (int i = 0; i < 4; ++i) out4[i] = v[i];
+    return VMX_OK;
+}
+
+int vmx_psnr_db(const double *mse, int n, int bpc, double psnr_max, double *psnr)
+{
+    if (!mse || !psnr || n < 0 || bpc < 8 || bpc > 16) return VMX_EINVAL;
+    const double peak = (double)((1 << bpc) - 1) / (double)(1 << (bpc - 8));
+    for (int i = 0; i < n; ++i) {
+        const double m = mse[i] > 1e-10 ? mse[i] : 1e-10;
+        double db = 10.0 * std::log10(peak * peak / m);
+        if (psnr_max > 0.0 && db > psnr_max) db = psnr_max;
+        psnr[i] = db;
+    }
+    return VMX_OK;
+}
+
+// ---------------------------------------------------- host-memory pipeline
+
+namespace {
+
+struct HostPlan {
+    size_t in_bytes;      // one plane of one chunk
+    size_t out_bytes;     // one chunk's outputs
+    size_t ws_bytes;      // the frame kernel's workspace for one chunk
+    size_t off_in[2][2];  // [slot][plane]
+    size_t off_out[2];
+    size_t off_ws;
+    size_t off_status;    // u32 status over all chunks
+    size_t total;
+    // Offsets inside one chunk's outputs.
+    size_t o_moments, o_s2_rows, o_psnr_rows, o_mse;
+};
+
+bool host_plan(int width, int height, int64_t stride, int bpc, int chunk, int features,
+               HostPlan *hp)
+{
+    Layout L;
+    if (chunk < 1 || !make_layout(width, height, bpc, chunk, features, &L)) return false;
+    if (stride < (int64_t)width * bytes_per_sample(bpc)) return false;
+    const size_t c = (size_t)chunk, H = (size_t)height;
+    hp->in_bytes = c * H * (size_t)stride;
+    size_t o = 0;
+    hp->o_moments = o;
+    o = align256(o + c * 4 * sizeof(double));
+    hp->o_s2_rows = o;
+    o = align256(o + c * 2 * H * sizeof(uint64_t));
+    hp->o_psnr_rows = o;
+    o = align256(o + c * H * sizeof(uint64_t));
+    hp->o_mse = o;
+    o = align256(o + c * sizeof(double));
+    hp->out_bytes = o;
+    hp->ws_bytes = L.total;
+    size_t off = 0;
+    for (int s = 0; s < 2; ++s)
+        for (int pl = 0; pl < 2; ++pl) {
+            hp->off_in[s][pl] = off;
+            off = align256(off + hp->in_bytes);
+        }
+    for (int s = 0; s < 2; ++s) {
+        hp->off_out[s] = off;
+        off = align256(off + hp->out_bytes);
+    }
+    hp->off_ws = off;
+    off = align256(off + hp->ws_bytes);
+    hp->off_status = off;
+    off = align256(off + sizeof(uint32_t));
+    hp->total = off;
+    return true;
+}
+
+}  // namespace
+
+size_t vmx_host_workspace_bytes(int width, int height, int64_t stride_bytes, int bpc,
+                                int chunk_frames, int features)
+{
+    HostPlan hp;
+    if (!host_plan(width, height, stride_bytes, bpc, chunk_frames, features, &hp)) return 0;
+    return hp.total;
+}
+
+void vmx_frames_host_traffic(int width, int height, int64_t stride_bytes, int bpc,
+                             int nframes, int features, int want_s2_rows,
+                             uint64_t *h2d_bytes, uint64_t *d2h_bytes)
+{
+    const uint64_t F = (uint64_t)std::max(nframes, 0), H = (uint64_t)std::max(height, 0);
+    (void)width;
+    (void)bpc;
+    if (h2d_bytes) *h2d_bytes = 2 * F * H * (uint64_t)std::max<int64_t>(stride_bytes, 0);
+    uint64_t out = 0;
+    if (features & VMX_FEATURE_MOMENT) {
+        out += F * 4 * sizeof(double);
+        if (want_s2_rows) out += F * 2 * H * sizeof(uint64_t);
+    }
+    if (features & VMX_FEATURE_PSNR) out += F * H * sizeof(uint64_t) + F * sizeof(double);
+    if (d2h_bytes) *d2h_bytes = out;
+}
+
+int vmx_frames_host(const void *ref, const void *dis, int width, int height,
+                    int64_t stride_bytes, int bpc, int nframes, int features,
+                    double *moments, uint64_t *s2_rows, uint64_t *psnr_rows, double *mse,
+                    double *psnr, double psnr_max, int chunk_frames, void *workspace,
+                    size_t workspace_bytes, void *stream)
+{
+    if (!ref || !dis || nframes < 1 || features < 1 || features > 3) return VMX_EINVAL;
+    const bool m = features & VMX_FEATURE_MOMENT, ps = features & VMX_FEATURE_PSNR;
+    if ((m && !moments) || (ps && (!psnr_rows || !mse)) || (psnr && !ps)) return VMX_EINVAL;
+    const int chunk = std::min(std::max(chunk_frames, 1), nframes);
+    HostPlan hp;
+    if (!host_plan(width, height, stride_bytes, bpc, chunk, features, &hp)) return VMX_EINVAL;
+    const bool own = workspace == nullptr;
+    if (!own && (workspace_bytes < hp.total || (uintptr_t)workspace % 256)) return VMX_EINVAL;
+    if (fail_at("alloc")) return VMX_ENOMEM;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaStream_t copy = nullptr;
+    cudaEvent_t copied[2] = {nullptr, nullptr}, computed[2] = {nullptr, nullptr};
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    int status = VMX_OK;
+    cudaError_t err = cudaSuccess;
+    if (own) {
+        void *p = nullptr;
+        err = cudaMalloc(&p, hp.total);
+        if (err != cudaSuccess) return cuda_fail(err);
+        ws = static_cast<unsigned char *>(p);
+    }
+    err = cudaStreamCreateWithFlags(&copy, cudaStreamNonBlocking);
+    for (int s = 0; s < 2 && err == cudaSuccess; ++s) {
+        err = cudaEventCreateWithFlags(&copied[s], cudaEventDisableTiming);
+        if (err == cudaSuccess) err = cudaEventCreateWithFlags(&computed[s], cudaEventDisableTiming);
+    }
+    uint32_t *dstatus = reinterpret_cast<uint32_t *>(ws + hp.off_status);
+    if (err == cudaSuccess) err = cudaMemsetAsync(dstatus, 0, sizeof(uint32_t), cs);
+    const size_t H = (size_t)height;
+    const size_t frame_bytes = H * (size_t)stride_bytes;
+    for (int c0 = 0, it = 0; c0 < nframes && err == cudaSuccess && status == VMX_OK;
+         c0 += chunk, ++it) {
+        const int n = std::min(chunk, nframes - c0);
+        const int slot = it & 1;
+        unsigned char *in_r = ws + hp.off_in[slot][0], *in_d = ws + hp.off_in[slot][1];
+        unsigned char *out = ws + hp.off_out[slot];
+        // Inputs of this chunk: wait until the slot's previous chunk computed.
+        if (it >= 2) err = cudaStreamWaitEvent(copy, computed[slot], 0);
+        if (err == cudaSuccess)
+            err = cudaMemcpyAsync(in_r, static_cast<const unsigned char *>(ref) + c0 * frame_bytes,
+                                  n * frame_bytes, cudaMemcpyHostToDevice, copy);
+        if (err == cudaSuccess)
+            err = cudaMemcpyAsync(in_d, static_cast<const unsigned char *>(dis) + c0 * frame_bytes,
+                                  n * frame_bytes, cudaMemcpyHostToDevice, copy);
+        if (err == cudaSuccess) err = cudaEventRecord(copied[slot], copy);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(cs, copied[slot], 0);
+        if (err != cudaSuccess) break;
+        Outputs o;
+        o.moments = m ? reinterpret_cast<double *>(out + hp.o_moments) : nullptr;
+        o.s2_rows = m ? reinterpret_cast<uint64_t *>(out + hp.o_s2_rows) : nullptr;
+        o.s2_sums = nullptr;
+        o.psnr_rows = ps ? reinterpret_cast<uint64_t *>(out + hp.o_psnr_rows) : nullptr;
+        o.mse = ps ? reinterpret_cast<double *>(out + hp.o_mse) : nullptr;
+        o.noise_sums = nullptr;
+        status = run_frames(in_r, in_d, width, height, stride_bytes, bpc, n, features, o,
+                            ws + hp.off_ws, hp.ws_bytes, cs, dstatus);
+        if (status != VMX_OK) break;
+        if (m) {
+            err = cudaMemcpyAsync(moments + (size_t)c0 * 4, o.moments, n * 4 * sizeof(double),
+                                  cudaMemcpyDeviceToHost, cs);
+            if (err == cudaSuccess && s2_rows)
+                err = cudaMemcpyAsync(s2_rows + (size_t)c0 * 2 * H, o.s2_rows,
+                                      n * 2 * H * sizeof(uint64_t), cudaMemcpyDeviceToHost, cs);
+        }
+        if (ps && err == cudaSuccess) {
+            err = cudaMemcpyAsync(psnr_rows + (size_t)c0 * H, o.psnr_rows, n * H * sizeof(uint64_t),
+                                  cudaMemcpyDeviceToHost, cs);
+            if (err == cudaSuccess)
+                err = cudaMemcpyAsync(mse + c0, o.mse, n * sizeof(double), cudaMemcpyDeviceToHost, cs);
+        }
+        if (err == cudaSuccess) err = cudaEventRecord(computed[slot], cs);
+    }
+    // A bounded wait that gave up in any chunk fails the call.
+    uint32_t st = 0;
+    if (err == cudaSuccess && status == VMX_OK)
+        err = cudaMemcpyAsync(&st, dstatus, sizeof st, cudaMemcpyDeviceToHost, cs);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(cs);
+    if (err == cudaSuccess && status == VMX_OK && st) status = VMX_ETIMEOUT;
+    if (copy) cudaStreamSynchronize(copy);
+    for (int s = 0; s < 2; ++s) {
+        if (copied[s]) cudaEventDestroy(copied[s]);
+        if (computed[s]) cudaEventDestroy(computed[s]);
+    }
+    if (copy) cudaStreamDestroy(copy);
+    if (own) cudaFree(ws);
+    if (status == VMX_OK && err != cudaSuccess) status = cuda_fail(err);
+    if (status == VMX_OK && psnr) status = vmx_psnr_db(mse, nframes, bpc, psnr_max, psnr);
+    return status;
+}
+
+}  // extern "C"

@@ -70,45 +70,62 @@ size_t vmx_workspace_bytes(int width, int height, int bpc, int nframes, int feat
  *   s2_rows       device or NULL, [nframes][2][height] uint64: each row's
  *                 exact sum of the binary32 squares in units (ref rows, then
  *                 dis rows).
+ *   s2_sums       device or NULL, [nframes][2] uint64: the CPU's rounded
+ *                 second-moment accumulators after the last pixel, in units
+ *                 (the doubles the CPU divides by the pixel count, exactly).
  *   workspace     device memory of at least vmx_workspace_bytes(...,
- *                 VMX_FEATURE_MOMENT) bytes, caller-owned; or NULL, in which
- *                 case the call allocates and frees it on `stream`.
- * Asynchronous on `stream`. A bounded device wait that gives up is reported
- * by vmx_workspace_status() on the same workspace.
+ *                 VMX_FEATURE_MOMENT) bytes, caller-owned and 256-byte
+ *                 aligned; or NULL, in which case the call allocates it on
+ *                 `stream`, waits for the result, frees it and returns the
+ *                 device status itself (the call is then synchronous).
+ * Asynchronous on `stream` when a workspace is given. A bounded device wait
+ * that gave up is reported by vmx_workspace_status() on that workspace.
  */
 int vmx_moment_frames(const void *ref, const void *dis, int width, int height,
                       int64_t stride_bytes, int bpc, int nframes, double *moments,
-                      uint64_t *s2_rows, void *workspace, size_t workspace_bytes,
-                      void *stream);
+                      uint64_t *s2_rows, uint64_t *s2_sums, void *workspace,
+                      size_t workspace_bytes, void *stream);
 
 /*
  * float_psnr of nframes frame pairs (ADR-1499).
- *   rows   device, [nframes][height] uint64: each row's exact sum of the
- *          binary32 squared differences in units of 1/scaler^2.
- *   mse    device, [nframes] doubles: the CPU's row-order noise / pixels.
+ *   rows        device, [nframes][height] uint64: each row's exact sum of the
+ *               binary32 squared differences in units of 1/scaler^2.
+ *   mse         device, [nframes] doubles: the CPU's row-order noise / pixels.
+ *   noise_sums  device or NULL, [nframes] uint64: the CPU's row-order noise
+ *               accumulator in units.
  * The PSNR itself is a host function of the MSE: vmx_psnr_db().
  * Workspace, stream and errors as vmx_moment_frames().
  */
 int vmx_float_psnr_frames(const void *ref, const void *dis, int width, int height,
                           int64_t stride_bytes, int bpc, int nframes, uint64_t *rows,
-                          double *mse, void *workspace, size_t workspace_bytes,
-                          void *stream);
+                          double *mse, uint64_t *noise_sums, void *workspace,
+                          size_t workspace_bytes, void *stream);
 
 /*
  * Both features in one read of both planes. Same arguments as the two calls
  * above; the workspace is vmx_workspace_bytes(..., VMX_FEATURE_MOMENT |
- * VMX_FEATURE_PSNR). Outputs as above; s2_rows may be NULL.
+ * VMX_FEATURE_PSNR). Outputs as above; s2_rows, s2_sums and noise_sums may
+ * be NULL.
  */
 int vmx_moment_psnr_frames(const void *ref, const void *dis, int width, int height,
                            int64_t stride_bytes, int bpc, int nframes, double *moments,
-                           uint64_t *s2_rows, uint64_t *psnr_rows, double *mse,
-                           void *workspace, size_t workspace_bytes, void *stream);
+                           uint64_t *s2_rows, uint64_t *s2_sums, uint64_t *psnr_rows,
+                           double *mse, uint64_t *noise_sums, void *workspace,
+                           size_t workspace_bytes, void *stream);
 
 /*
  * Status of the last call that used `workspace`: VMX_OK, or VMX_ETIMEOUT if a
  * bounded device wait gave up. Synchronises `stream`.
  */
 int vmx_workspace_status(const void *workspace, void *stream);
+
+/*
+ * How the last call on `workspace` formed its second-moment sums, summed over
+ * its frames and planes (host array of 4): rows added exactly, rows added by
+ * their run, rows walked term by term, and 2048-term chunks the term walk
+ * scanned (including the psnr row walk). Synchronises `stream`.
+ */
+int vmx_workspace_stats(const void *workspace, void *stream, uint64_t *out4);
 
 /*
  * PSNR in dB from the MSE on the 8-bit scale, on the host:
@@ -119,22 +136,30 @@ int vmx_workspace_status(const void *workspace, void *stream);
 int vmx_psnr_db(const double *mse, int n, int bpc, double psnr_max, double *psnr);
 
 /*
- * Host-memory entry point: frames in host memory (pinned recommended),
- * results in host memory. Copies chunks of `chunk_frames` frames to the
- * device on `stream` while the previous chunk computes on a second stream
- * the library creates, then copies the results back. Synchronises before it
- * returns. features: VMX_FEATURE_* bits; outputs of a feature not asked for
- * may be NULL, as may s2_rows and psnr (psnr needs VMX_FEATURE_PSNR).
- *   workspace  device memory of vmx_host_workspace_bytes(...) bytes, or NULL
- *              (then allocated and freed by the call).
+ * Host-memory entry point: frames in host memory (page-locked memory lets
+ * the copies overlap the kernels), results in host memory, same layout and
+ * outputs as the device calls. Chunks of `chunk_frames` frames are copied to
+ * the device on a stream the call creates while the previous chunk computes
+ * on `stream`; each chunk's results are copied back on `stream`. Returns
+ * after everything has finished. features: VMX_FEATURE_* bits; outputs of a
+ * feature not asked for may be NULL, as may s2_rows and psnr (psnr needs
+ * VMX_FEATURE_PSNR; it is vmx_psnr_db() of mse with psnr_max).
+ *   workspace  device memory of vmx_host_workspace_bytes(...) bytes, 256-byte
+ *              aligned, or NULL (then allocated and freed by the call).
  */
-size_t vmx_host_workspace_bytes(int width, int height, int bpc, int chunk_frames,
-                                int features);
+size_t vmx_host_workspace_bytes(int width, int height, int64_t stride_bytes, int bpc,
+                                int chunk_frames, int features);
 int vmx_frames_host(const void *ref, const void *dis, int width, int height,
                     int64_t stride_bytes, int bpc, int nframes, int features,
                     double *moments, uint64_t *s2_rows, uint64_t *psnr_rows, double *mse,
                     double *psnr, double psnr_max, int chunk_frames, void *workspace,
                     size_t workspace_bytes, void *stream);
+
+/* Bytes of host<->device traffic one vmx_frames_host() call moves for these
+ * arguments (inputs in, outputs out), for reporting. */
+void vmx_frames_host_traffic(int width, int height, int64_t stride_bytes, int bpc,
+                             int nframes, int features, int want_s2_rows,
+                             uint64_t *h2d_bytes, uint64_t *d2h_bytes);
 
 /* Name of a status code (and the last CUDA error for VMX_ECUDA). */
 const char *vmx_strerror(int status);

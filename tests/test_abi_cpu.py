@@ -1,0 +1,119 @@
+"""libvmx loads, exports every symbol include/vmx.h declares, and its host
+logic behaves, all without a GPU (no compute call reaches the device)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from exact_reductions_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "vmx.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vmx_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_lib()
+    return _lib.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert names == sorted(_lib.SIGNATURES)
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"{name} has no binding"
+
+
+def test_version_and_strerror(lib):
+    assert lib.vmx_version() == 10000
+    for code in (0, -1, -2, -3, -4):
+        assert lib.vmx_strerror(code)
+    assert lib.vmx_strerror(-99) == b"unknown status"
+
+
+@pytest.mark.parametrize("args", [
+    (0, 16, 16, 1, 3), (32769, 1, 16, 1, 3), (16, 0, 16, 1, 3), (16, 16, 7, 1, 3),
+    (16, 16, 17, 1, 3), (16, 16, 16, 0, 3), (16, 16, 16, 1, 0), (16, 16, 16, 1, 4),
+    (8192, 8192, 16, 1, 3)])
+def test_workspace_rejects_bad_shapes(lib, args):
+    assert lib.vmx_workspace_bytes(*args) == 0
+
+
+def test_workspace_sizes(lib):
+    small = lib.vmx_workspace_bytes(320, 240, 8, 1, 3)
+    assert small > 0 and small % 256 == 0
+    # Frames above 2^21 pixels with second moments carry per-row records.
+    a = lib.vmx_workspace_bytes(3840, 2160, 16, 16, 3)
+    b = lib.vmx_workspace_bytes(3840, 2160, 16, 16, 2)
+    assert a > b + 16 * 2 * 2160 * 16
+    assert lib.vmx_workspace_bytes(3840, 2160, 16, 32, 3) > a
+
+
+def test_argument_errors_launch_nothing(lib):
+    """Bad arguments come back as VMX_EINVAL before any CUDA call."""
+    launches = lib.vmx_kernel_launches()
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.addressof(buf)
+    E = _lib.VMX_EINVAL
+    # null planes, stride too small, odd uint16 stride, bpc out of range
+    assert lib.vmx_moment_frames(None, p, 4, 4, 8, 16, 1, p, None, None, p, 1 << 20, None) == E
+    assert lib.vmx_moment_frames(p, p, 4, 4, 6, 16, 1, p, None, None, p, 1 << 20, None) == E
+    assert lib.vmx_moment_frames(p, p, 4, 4, 9, 16, 1, p, None, None, p, 1 << 20, None) == E
+    assert lib.vmx_moment_frames(p, p, 4, 4, 8, 17, 1, p, None, None, p, 1 << 20, None) == E
+    # missing outputs, zero frames, workspace too small
+    assert lib.vmx_moment_frames(p, p, 4, 4, 8, 16, 1, None, None, None, p, 1 << 20, None) == E
+    assert lib.vmx_float_psnr_frames(p, p, 4, 4, 8, 16, 1, None, p, None, p, 1 << 20, None) == E
+    assert lib.vmx_moment_psnr_frames(p, p, 4, 4, 8, 16, 0, p, None, None, p, p, None, p,
+                                      1 << 20, None) == E
+    aligned = (p + 255) & ~255
+    assert lib.vmx_moment_frames(p, p, 4, 4, 8, 16, 1, p, None, None, aligned, 16, None) == E
+    assert lib.vmx_frames_host(None, p, 4, 4, 8, 16, 1, 3, p, None, p, p, None, 0.0, 1, None, 0,
+                               None) == E
+    assert lib.vmx_kernel_launches() == launches
+
+
+def test_injected_launch_failure(lib, monkeypatch):
+    """VMX_TEST_FAIL_AT makes a stage fail on the host; the error surfaces."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    p = (ctypes.addressof(buf) + 255) & ~255
+    monkeypatch.setenv("VMX_TEST_FAIL_AT", "launch")
+    st = lib.vmx_moment_frames(p, p, 4, 4, 8, 16, 1, p, None, None, p, 1 << 15, None)
+    assert st == _lib.VMX_ECUDA and b"injected" in lib.vmx_strerror(st)
+    monkeypatch.setenv("VMX_TEST_FAIL_AT", "alloc")
+    st = lib.vmx_moment_frames(p, p, 4, 4, 8, 16, 1, p, None, None, None, 0, None)
+    assert st == _lib.VMX_ENOMEM
+    monkeypatch.setenv("VMX_TEST_FAIL_AT", "status")
+    assert lib.vmx_workspace_status(p, None) == _lib.VMX_ETIMEOUT
+    with pytest.raises(_lib.VmxError):
+        _lib.check(lib.vmx_workspace_status(p, None), "status")
+
+
+def test_psnr_db_matches_oracle(lib):
+    """The host PSNR step equals the oracle's on the same MSE values."""
+    rng = np.random.default_rng(11)
+    mse = np.concatenate([[0.0, 1e-12, 1e-10, 1.0], rng.uniform(0, 400, 200),
+                          10.0 ** rng.uniform(-9, 4, 200)])
+    for bpc in (8, 10, 12, 16):
+        for cap in (0.0, 60.0):
+            out = np.zeros_like(mse)
+            assert lib.vmx_psnr_db(mse.ctypes.data, mse.size, bpc, cap, out.ctypes.data) == 0
+            want = np.array([oracle.psnr_db(m, bpc, cap) for m in mse])
+            assert np.array_equal(out.view(np.uint64), want.view(np.uint64))
+
+
+def test_host_traffic(lib):
+    h2d, d2h = ctypes.c_uint64(), ctypes.c_uint64()
+    lib.vmx_frames_host_traffic(3840, 2160, 7680, 16, 16, 3, 0, ctypes.addressof(h2d),
+                                ctypes.addressof(d2h))
+    assert h2d.value == 2 * 16 * 2160 * 7680
+    assert d2h.value == 16 * 4 * 8 + 16 * 2160 * 8 + 16 * 8

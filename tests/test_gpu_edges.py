@@ -1,0 +1,112 @@
+"""Edge cases on the GPU: ragged widths, padded strides, misaligned planes,
+one-pixel rows and columns, the widest rows, the largest frames, repeated
+calls, and the host-memory entry point. Each compared with the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+from exact_reductions_gb300 import api, synth
+from gpu_helpers import oracle_frames, run_and_check, same_doubles, to_device, u64
+
+pytestmark = pytest.mark.gpu
+
+
+def _pair(seed, F, H, S, bpc, mode="uniform", W=None):
+    rng = np.random.default_rng(seed)
+    refs, diss = [], []
+    for _ in range(F):
+        r, d = synth.random_plane_pair(rng, W or S, H, bpc, stride_samples=S, mode=mode)
+        refs.append(r)
+        diss.append(d)
+    return np.stack(refs), np.stack(diss)
+
+
+@pytest.mark.parametrize("bpc", [8, 10, 12, 16])
+@pytest.mark.parametrize("W,H", [(1, 1), (1, 37), (37, 1), (7, 5), (255, 3), (257, 9),
+                                 (1000, 17), (2049, 11)])
+def test_ragged_shapes(W, H, bpc):
+    for mode in ("uniform", "extreme"):
+        ref, dis = _pair(W * 131 + H + bpc, 2, H, W, bpc, mode)
+        run_and_check(ref, dis, bpc)
+
+
+@pytest.mark.parametrize("bpc", [8, 16])
+def test_padded_stride_with_garbage(bpc):
+    """Samples past the width are garbage and must not count."""
+    W, S, H = 1000, 1024 + 8, 40
+    ref, dis = _pair(5, 3, H, S, bpc, W=W)
+    run_and_check(ref, dis, bpc, width=W)
+
+
+@pytest.mark.parametrize("bpc", [8, 16])
+def test_misaligned_planes(bpc):
+    """Planes 2 or 1 samples past a 16-byte boundary use scalar loads."""
+    ref, dis = _pair(6, 2, 64, 640, bpc)
+    run_and_check(ref, dis, bpc, misalign=1)
+
+
+def test_misaligned_past_2_53():
+    """The scalar-load path through runs and the walk (16-bit, 2560x1440)."""
+    wl = synth.WORKLOADS["T1"]
+    ref, dis = wl.batch()
+    run_and_check(ref, dis, 16, misalign=1)
+
+
+def test_widest_rows_largest_frame():
+    """32768-sample rows (2^15 terms, ADR-1499 "Decision" point 1) and a
+    2^25-pixel frame past 2^53 units."""
+    rng = np.random.default_rng(9)
+    ref = rng.integers(30000, 65536, size=(1, 1024, 32768), dtype=np.uint16)
+    dis = rng.integers(0, 65536, size=(1, 1024, 32768), dtype=np.uint16)
+    run_and_check(ref, dis, 16)
+
+
+def test_single_column_tall_frame():
+    """Width 1: every row is one term; frames of 2^21 + 1 pixels take the
+    look-back path with 64-row tiles."""
+    rng = np.random.default_rng(10)
+    H = (1 << 21) + 1
+    ref = rng.integers(60000, 65536, size=(1, H, 1), dtype=np.uint16)
+    dis = rng.integers(0, 65536, size=(1, H, 1), dtype=np.uint16)
+    run_and_check(ref, dis, 16)
+
+
+def test_repeated_calls_identical_and_workspace_reused():
+    wl = synth.WORKLOADS["T4"]
+    ref, dis = wl.batch()
+    r, d = to_device(ref), to_device(dis)
+    first = api.frames(r, d, 16, sums=True)
+    for _ in range(3):
+        again = api.frames(r, d, 16, sums=True, ws=first["_workspace"])
+        torch.cuda.synchronize()
+        assert torch.equal(again["moments"].view(torch.int64), first["moments"].view(torch.int64))
+        assert torch.equal(again["psnr_rows"].view(torch.int64),
+                           first["psnr_rows"].view(torch.int64))
+        assert torch.equal(again["s2_sums"].view(torch.int64), first["s2_sums"].view(torch.int64))
+
+
+def test_host_entry_matches_device_entry():
+    """vmx_frames_host (host buffers, copies inside the call, chunks of 2)
+    gives the device call's outputs, and the PSNR of the oracle's MSE."""
+    import oracle
+    wl = synth.WORKLOADS["C5a"]
+    ref, dis = wl.batch(5)
+    host = api.frames_host(ref, dis, 16, features=3, chunk_frames=2, s2_rows=True)
+    dev = api.frames(to_device(ref), to_device(dis), 16, s2_rows=True)
+    torch.cuda.synchronize()
+    assert same_doubles(host["moments"], dev["moments"].cpu().numpy())
+    assert np.array_equal(host["psnr_rows"], u64(dev["psnr_rows"]))
+    assert np.array_equal(host["s2_rows"], u64(dev["s2_rows"]))
+    assert same_doubles(host["mse"], dev["mse"].cpu().numpy())
+    want_mse = [w["mse"] for w in oracle_frames(ref, dis, 16, range(5))]
+    assert same_doubles(host["mse"], want_mse)
+    assert same_doubles(host["psnr"], [oracle.psnr_db(m, 16, 0.0) for m in want_mse])
+
+
+def test_launch_counter_counts_calls():
+    wl = synth.WORKLOADS["C1"]
+    ref, dis = wl.batch()
+    before = api.kernel_launches()
+    run_and_check(ref, dis, 8)
+    assert api.kernel_launches() == before + 1
