@@ -82,9 +82,105 @@ uint64_t apply_terms(uint64_t s, const uint32_t *t, int n, uint64_t *count)
     return s;
 }
 
+// The same walk step by step with the closed forms of binades 53 and 54
+// (closed_form_after) and single-term runs from 55 up.
+uint64_t apply_terms_cf(uint64_t s, const uint32_t *t, int n, uint64_t *count)
+{
+    for (int k = 0; k < n; ++k) {
+        const uint64_t x = s + t[k];
+        if (VMX_MUT(5) || x <= kTwo53) {
+            s = x;
+            continue;
+        }
+        if (s >= kTwo53) {
+            const int b = binade_of(s);
+            const uint64_t top = 2ull << b;
+            uint64_t next;
+            if (b <= 54) next = closed_form_after(s, t[k], t[k] & 1u, b);
+            else next = apply(run_of_term(t[k], b - 52), s, b - 52);
+            if (next < top) {
+                s = next;
+                continue;
+            }
+        }
+        s = (VMX_MUT(7) && s >= kTwo53) ? round_to_ulp(x, binade_of(s) - 52) : rnd53(x);
+    }
+    if (count) *count += (uint64_t)n;
+    return s;
+}
+
 }  // namespace
 
 extern "C" {
+
+// The CPU's second-moment sum through the closed-form route: per row the
+// exact sum and the count of odd terms; rows in binades 53 and 54 are added
+// in closed form, rows planned in binades from 55 up by their run, all other
+// rows term by term. stats as vmx_model_plane_s2.
+uint64_t vmx_model_plane_s2_cf(const uint16_t *plane, int w, int h, int64_t stride_samples,
+                               uint64_t *stats)
+{
+    Plane pl{plane, w, h, stride_samples};
+    std::vector<uint64_t> rows(h), odd(h);
+    std::vector<RowRec> rec(h);
+    uint64_t prefix = 0;
+    for (int i = 0; i < h; ++i) {
+        uint64_t s = 0, c = 0;
+        for (int j = 0; j < w; ++j) {
+            const uint32_t t = pl.term(i, j);
+            s += t;
+            c += t & 1u;
+        }
+        rows[i] = s;
+        odd[i] = c;
+        memset(&rec[i], 0, sizeof rec[i]);
+        const int e = plan_binade(prefix, s);
+        if (e >= 55) {
+            const Run r = row_run(pl, i, VMX_MUT(4) ? e - 51 : e - 52, s);
+            rec[i].inc0 = r.inc[0];
+            rec[i].dinc = (int32_t)(r.inc[1] - r.inc[0]);
+            rec[i].e = (uint8_t)e;
+            rec[i].kind = kRowRun;
+        }
+        prefix += s;
+    }
+    uint64_t st[4] = {0, 0, 0, 0};
+    uint64_t s = 0;
+    std::vector<uint32_t> t(w);
+    for (int i = 0; i < h; ++i) {
+        const uint64_t r = rows[i];
+        if (s + r <= kTwo53 || r == 0) {
+            s += r;
+            ++st[0];
+            continue;
+        }
+        if (s >= kTwo53) {
+            const int b = binade_of(s);
+            uint64_t next = 0;
+            bool have = false;
+            if (b <= 54) {
+                next = closed_form_after(s, r, odd[i], b);
+                have = true;
+            } else if (rec[i].kind == kRowRun && rec[i].e == b) {
+                Run run;
+                run.inc[0] = rec[i].inc0;
+                run.inc[1] = rec[i].inc0 + (uint64_t)(int64_t)rec[i].dinc;
+                next = apply(run, s, b - 52);
+                have = true;
+            }
+            if (have && next < (2ull << b)) {
+                s = next;
+                ++st[1];
+                continue;
+            }
+        }
+        for (int j = 0; j < w; ++j) t[j] = pl.term(i, j);
+        s = apply_terms_cf(s, t.data(), w, &st[3]);
+        ++st[2];
+    }
+    if (stats) memcpy(stats, st, sizeof st);
+    return s;
+}
 
 // The CPU's second-moment sum (units) of one 16-bit plane through the
 // library's steps. plan: 0 = plan from the exact prefix, 1 = a random binade

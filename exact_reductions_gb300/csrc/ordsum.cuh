@@ -272,6 +272,27 @@ VMX_HD LaneRun lane_run_fp(const uint32_t *t, int n, int sh)
     return r;
 }
 
+// Closed forms for the binades 53 and 54. Every term of this method is the
+// binary32 square of a codeword (or of a difference of codewords) below 2^16,
+// and every such square t satisfies t mod 8 in {0, 1, 4}, with t odd exactly
+// when the codeword is odd and below 4096 (checked over all 65 536 codewords).
+// So under last place 2 (binade 53) a term is either a multiple of 4 (added
+// exactly, parity kept) or a tie that lands S on a multiple of 4: from an
+// even start every tie rounds down by 1; from an odd start the first tie
+// rounds up by 1 and the rest down. Under last place 4 (binade 54) the
+// residues 0 and 4 add exactly and residue 1 rounds down, for either parity.
+// With `sum` the exact sum of a run of such terms and `odd` how many of them
+// are odd, the run adds:
+//   binade 53: sum - odd, plus 2 when the start is odd and odd > 0;
+//   binade 54: sum - odd.
+VMX_HD uint64_t closed_form_after(uint64_t s, uint64_t sum, uint64_t odd, int binade)
+{
+    if (VMX_MUT(2)) return s + sum - odd;  // parity ignored
+    uint64_t r = s + sum - odd;
+    if (binade == 53 && odd > 0 && ((s >> 1) & 1ull)) r += 2;
+    return r;
+}
+
 // Kinds of per-row record the streaming pass leaves for the walk.
 enum RowKind : uint8_t {
     kRowNone = 0,  // no run: the walk adds the row exactly or from its terms

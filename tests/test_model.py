@@ -28,6 +28,8 @@ def model():
         u64, i32, i64, vp = ctypes.c_uint64, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
         lib.vmx_model_plane_s2.argtypes = [vp, i32, i32, i64, i32, u64, vp]
         lib.vmx_model_plane_s2.restype = u64
+        lib.vmx_model_plane_s2_cf.argtypes = [vp, i32, i32, i64, vp]
+        lib.vmx_model_plane_s2_cf.restype = u64
         lib.vmx_model_ordered_terms.argtypes = [vp, i32, u64]
         lib.vmx_model_ordered_terms.restype = u64
         lib.vmx_model_run_of_terms.argtypes = [vp, i32, i32, vp]
@@ -42,10 +44,15 @@ def model():
 
 
 def plane_s2(plane, plan=0, seed=1):
+    """plan 0/1/2: real, random or no plans with general runs; 3: the
+    closed-form route (binades 53/54 in closed form, runs from 55 up)."""
     plane = np.ascontiguousarray(plane, dtype=np.uint16)
     h, w = plane.shape
     stats = np.zeros(4, dtype=np.uint64)
-    s = model().vmx_model_plane_s2(plane.ctypes.data, w, h, w, plan, seed, stats.ctypes.data)
+    if plan == 3:
+        s = model().vmx_model_plane_s2_cf(plane.ctypes.data, w, h, w, stats.ctypes.data)
+    else:
+        s = model().vmx_model_plane_s2(plane.ctypes.data, w, h, w, plan, seed, stats.ctypes.data)
     return int(s), stats
 
 
@@ -135,6 +142,21 @@ def test_model_real_plans_match_oracle():
     check_frames(plans=(0,))
 
 
+def test_model_closed_forms_match_oracle():
+    """Binades 53 and 54 in closed form from (row sum, odd count)."""
+    check_frames(plans=(3,))
+
+
+def test_closed_form_residues_of_all_codewords():
+    """The fact the closed forms rest on: every binary32 square of a codeword
+    is 0, 1 or 4 mod 8, and odd exactly for odd codewords below 4096."""
+    from exact import rnd24
+    p = np.arange(65536, dtype=np.uint64)
+    t = rnd24(p * p)
+    assert set((t % 8).tolist()) == {0, 1, 4}
+    assert np.array_equal((t & 1) == 1, ((p & 1) == 1) & (p < 4096))
+
+
 def test_model_wrong_and_no_plans_match_oracle():
     check_frames(plans=(1, 2), names=("T1", "C4", "T4a", "C5b2", "T3"))
 
@@ -170,6 +192,6 @@ def test_planted_break_fails(k):
     m.vmx_model_set_mutation(k)
     try:
         with pytest.raises(AssertionError):
-            check_frames(plans=(0, 2), names=("C4", "T4a", "T4b", "C5b2", "T3", "C5c"))
+            check_frames(plans=(0, 2, 3), names=("C4", "T4a", "T4b", "C5b2", "T3", "C5c"))
     finally:
         m.vmx_model_set_mutation(0)
