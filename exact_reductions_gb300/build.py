@@ -27,7 +27,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 CU_SOURCES = ["vmx_kernels.cu"]
 CPP_SOURCES = ["vmx_abi.cpp"]
-HEADERS = ["ordsum.cuh", "vmx_internal.h", "vmx_kernels.cuh"]
+HEADERS = ["ordsum.cuh", "vmx_internal.h"]
 
 LIB = os.path.join(BUILD, "libvmx.so")
 MODEL = os.path.join(BUILD, "libvmx_model.so")

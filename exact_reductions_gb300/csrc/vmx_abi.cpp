@@ -47,35 +47,41 @@ bool make_layout(int width, int height, int bpc, int frames, int features, Layou
         return false;
     if ((int64_t)width * height > (int64_t)1 << 25) return false;
     if (features < 1 || features > 3) return false;
-    const int rows_per_warp = std::max(1, (2048 + width - 1) / width);
-    const int rpt = std::min(kMaxRowsPerTile, kWarps * rows_per_warp);
-    const int tpf = (height + rpt - 1) / rpt;
-    if ((int64_t)frames * tpf >= (int64_t)INT_MAX / 2) return false;
-    const size_t F = (size_t)frames, T = (size_t)tpf, H = (size_t)height;
+    const int rpi = std::min(kMaxRowsPerItem, std::max(1, (kItemPixels + width - 1) / width));
+    const int ipf = (height + rpi - 1) / rpi;
+    const int bpf = (ipf + kBlockItems - 1) / kBlockItems;
+    if ((int64_t)frames * ipf >= (int64_t)INT_MAX / 2) return false;
+    const size_t F = (size_t)frames, I = (size_t)ipf, B = (size_t)bpf, H = (size_t)height;
+    const int64_t n = (int64_t)width * height;
+    const bool m = features & VMX_FEATURE_MOMENT;
     L->width = width;
     L->height = height;
     L->frames = frames;
     L->bpc = bpc;
     L->features = features;
-    L->rows_per_tile = rpt;
-    L->tiles_per_frame = tpf;
-    L->ordered = bpc > 8 && (int64_t)width * height > ((int64_t)1 << 21) &&
-                 (features & VMX_FEATURE_MOMENT);
+    L->rows_per_item = rpi;
+    L->items_per_frame = ipf;
+    L->blocks_per_frame = bpf;
+    // Terms are below 2^32 units: a frame of n pixels stays at or below 2^53
+    // units when n <= 2^21 and below 2^55 when n <= 2^23.
+    L->ordered = m && bpc > 8 && n > ((int64_t)1 << 21);
+    L->full = L->ordered && n > ((int64_t)1 << 23);
     size_t off = 0;
     L->off_ctrl = off;
-    L->ctrl_bytes = (kCtrlWords + F + F * T) * sizeof(uint32_t);
+    L->ctrl_bytes = (kCtrlWords + F + F * B + (L->full ? F * I : 0)) * sizeof(uint32_t);
     off = align256(off + L->ctrl_bytes);
-    L->off_tile_agg = off;
-    off = align256(off + F * T * 2 * sizeof(uint64_t));
-    L->off_tile_inc = off;
-    off = align256(off + F * T * 2 * sizeof(uint64_t));
-    L->off_tile_s1 = off;
-    off = align256(off + F * T * 2 * sizeof(uint64_t));
+    L->off_items = off;
+    off = align256(off + F * I * sizeof(Agg));
+    L->off_blocks = off;
+    off = align256(off + F * B * sizeof(Agg));
+    L->off_item_inc = off;
+    if (L->full) off = align256(off + F * I * 2 * sizeof(uint64_t));
     L->off_s2_rows = off;
-    if (features & VMX_FEATURE_MOMENT) off = align256(off + F * 2 * H * sizeof(uint64_t));
-    L->off_psnr_rows = off;
+    if (m) off = align256(off + F * 2 * H * sizeof(uint64_t));
+    L->off_odd_rows = off;
+    if (L->ordered) off = align256(off + F * 2 * H * sizeof(uint32_t));
     L->off_rec = off;
-    if (L->ordered) off = align256(off + F * 2 * H * sizeof(RowRec));
+    if (L->full) off = align256(off + F * 2 * H * sizeof(RowRec));
     L->total = off;
     return true;
 }
@@ -125,15 +131,18 @@ int run_frames(const void *ref, const void *dis, int width, int height, int64_t 
     p.height = height;
     p.frames = nframes;
     p.k = bpc - 8;
-    p.rows_per_tile = L.rows_per_tile;
-    p.tiles_per_frame = L.tiles_per_frame;
+    p.rows_per_item = L.rows_per_item;
+    p.items_per_frame = L.items_per_frame;
+    p.blocks_per_frame = L.blocks_per_frame;
     p.ctrl = reinterpret_cast<uint32_t *>(ws + L.off_ctrl);
     p.done = p.ctrl + kCtrlWords;
-    p.flags = p.done + nframes;
+    p.block_done = p.done + nframes;
+    p.flags = p.block_done + (size_t)nframes * L.blocks_per_frame;
     p.status = status_word ? status_word : p.ctrl + kCtrlStatus;
-    p.tile_agg = reinterpret_cast<uint64_t *>(ws + L.off_tile_agg);
-    p.tile_inc = reinterpret_cast<uint64_t *>(ws + L.off_tile_inc);
-    p.tile_s1 = reinterpret_cast<uint64_t *>(ws + L.off_tile_s1);
+    p.items = reinterpret_cast<Agg *>(ws + L.off_items);
+    p.blocks = reinterpret_cast<Agg *>(ws + L.off_blocks);
+    p.item_inc = reinterpret_cast<uint64_t *>(ws + L.off_item_inc);
+    p.odd_rows = reinterpret_cast<uint32_t *>(ws + L.off_odd_rows);
     p.s2_rows = o.s2_rows ? o.s2_rows : reinterpret_cast<uint64_t *>(ws + L.off_s2_rows);
     p.psnr_rows = o.psnr_rows;
     p.rec = reinterpret_cast<RowRec *>(ws + L.off_rec);

@@ -11,35 +11,57 @@
 
 namespace vmx {
 
-constexpr int kThreads = 256;              // threads per CTA
-constexpr int kWarps = kThreads / 32;      // one row at a time per warp
-constexpr int kMaxRowsPerTile = 64;        // rows a CTA takes per ticket, at most
-constexpr int kUnroll = 4;                 // 256-pixel segments in flight per warp
+constexpr int kThreads = 256;              // threads per CTA (8 independent warps)
+constexpr int kWarps = kThreads / 32;
+#ifndef VMX_MIN_BLOCKS
+#define VMX_MIN_BLOCKS 3
+#endif
+#ifndef VMX_UNROLL
+#define VMX_UNROLL 4
+#endif
+constexpr int kMinBlocks = VMX_MIN_BLOCKS; // CTAs per SM the kernel is compiled for
+constexpr int kMaxRowsPerItem = 32;        // rows a warp takes per ticket, at most
+constexpr int kItemPixels = 4096;          // target pixels per warp item
+constexpr int kUnroll = VMX_UNROLL;        // 16-byte vectors in flight per lane per plane
 constexpr uint32_t kSpinLimit = 1u << 22;  // bounded look-back wait (polls)
 
 // Control words at the start of the workspace (cleared before each call).
 enum Ctrl : int {
-    kCtrlTicket = 0,     // next tile ticket
+    kCtrlTicket = 0,     // next item ticket
     kCtrlStatus = 1,     // 0, or 1 when a bounded wait gave up
     kCtrlRowsExact = 2,  // walk statistics: rows added exactly
-    kCtrlRowsRun = 3,    //   rows added by their run
+    kCtrlRowsRun = 3,    //   rows added by a closed form or a run
     kCtrlRowsTerms = 4,  //   rows walked term by term
-    kCtrlTermChunks = 5, //   2048-term chunks the term walk scanned
+    kCtrlPasses = 5,     //   search passes and chunks the walks scanned
+    kCtrlWalkTicket = 6, // next frame to walk
     kCtrlWords = 8,
 };
+
+// Per-item and per-block sums the walk reads (64 bytes): the exact
+// second-moment sums (ref, dis), the first-moment sums, the psnr sum, and the
+// odd-term counts (ref in the low half of odd, dis in the high half).
+struct alignas(16) Agg {
+    uint64_t s2[2];
+    uint64_t s1[2];
+    uint64_t psnr;
+    uint64_t odd;
+    uint64_t pad[2];
+};
+constexpr int kBlockItems = 32;  // items folded into one block aggregate
 
 // Where everything lives in the workspace. All offsets are 256-byte aligned.
 struct Layout {
     int width, height, frames, bpc, features;
-    int rows_per_tile, tiles_per_frame;
-    bool ordered;        // second moments may pass 2^53 units: look-back + runs
-    size_t off_ctrl;     // u32 [kCtrlWords] + done[F] + flag[F * T]
+    int rows_per_item, items_per_frame, blocks_per_frame;
+    bool ordered;        // second moments may pass 2^53 units: odd counts per row
+    bool full;           // ... and 2^55: look-back and row runs from binade 55 up
+    size_t off_ctrl;     // u32 [kCtrlWords] + done[F] + block_done[F * B] + flag[F * I]
     size_t ctrl_bytes;   // bytes cleared per call
-    size_t off_tile_agg; // u64 [F * T][2] exact second-moment sums per tile
-    size_t off_tile_inc; // u64 [F * T][2] inclusive exact prefix per tile
-    size_t off_tile_s1;  // u64 [F * T][2] first-moment sums per tile
+    size_t off_items;    // Agg [F * I]
+    size_t off_blocks;   // Agg [F * B]
+    size_t off_item_inc; // u64 [F * I][2] inclusive exact prefix per item (look-back)
     size_t off_s2_rows;  // u64 [F][2][H] (when the caller passes none)
-    size_t off_psnr_rows;// u64 [F][H]    (when the caller passes none)
+    size_t off_odd_rows; // u32 [F][2][H] odd terms per row
     size_t off_rec;      // RowRec [F][2][H]
     size_t total;
 };
@@ -53,11 +75,13 @@ struct Params {
     int64_t pitch;    // bytes between frames
     int width, height, frames;
     int k;            // bpc - 8
-    int rows_per_tile, tiles_per_frame;
-    uint32_t *ctrl, *done, *flags;
+    int rows_per_item, items_per_frame, blocks_per_frame;
+    uint32_t *ctrl, *done, *block_done, *flags;
     uint32_t *status;  // set to 1 when a bounded wait gives up
-    uint64_t *tile_agg, *tile_inc, *tile_s1;
+    Agg *items, *blocks;
+    uint64_t *item_inc;
     uint64_t *s2_rows, *psnr_rows;
+    uint32_t *odd_rows;
     RowRec *rec;
     double *moments, *mse;
     uint64_t *s2_sums, *noise_sums;

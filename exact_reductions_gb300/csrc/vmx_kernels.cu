@@ -2,26 +2,30 @@
 // of frame pairs, every sum an exact integer in units of 1/scaler^2, and the
 // CPU's rounded double sums reproduced value for value.
 //
-// One persistent kernel per call. CTAs take tiles (a few whole rows of one
-// frame, both planes) from a ticket counter, in frame-major row order:
+// One persistent kernel per call; every warp works on its own. A warp takes
+// an item (a few whole rows of one frame, both planes) from a ticket counter,
+// in frame-major row order, with no CTA barrier anywhere:
 //
-//   A. Stream the tile's rows once with coalesced 16-byte loads and form each
-//      row's exact sums: first moments (sum of p), second-moment terms
-//      (binary32 squares, ADR-1497 "Context") and psnr terms (binary32 squares
-//      of the differences, ADR-1499 "Context"). No float partials, no atomics.
-//   B. Second moments that may pass 2^53 units (frames above 2^21 pixels):
-//      publish the tile's exact sums and learn the exact sum before the tile
-//      by a decoupled look-back over the earlier tiles of the frame (bounded
-//      wait). If the plane is past 2^53 there, plan each row's binade from
-//      that exact prefix and form the row's run (ADR-1497 "Decision", third
-//      point) from 256-pixel segments of 32 lanes x 8 pixels, re-reading the
-//      rows just streamed (L2 hits).
-//   C. The CTA that finishes a frame's last tile walks that frame while the
-//      others stream on: each plane's rows are added exactly, by their runs,
-//      or term by term where a row crosses a binade or its plan was wrong
-//      (the check of ADR-1497 "Decision"), all as CTA-parallel scans; the
-//      psnr noise adds the exact row sums in row order the same way
-//      (ADR-1499 "Decision"). It writes the doubles the CPU divides out.
+//   A. It streams the item's rows once with coalesced 16-byte loads and forms
+//      each row's exact sums: first moments (sum of p), second-moment terms
+//      (binary32 squares, ADR-1497 "Context"), psnr terms (binary32 squares of
+//      the differences, ADR-1499 "Context") and, when the second moments can
+//      pass 2^53 units, the number of odd terms per row. No float partials,
+//      no atomics on data.
+//   B. Only for frames above 2^23 pixels, whose sums can pass 2^55 units: the
+//      item's exact sums are published and the exact sum before the item is
+//      read by a decoupled look-back over the frame's earlier items (bounded
+//      wait). Rows planned in a binade from 55 up get their run (ADR-1497
+//      "Decision", third point) from 256-pixel segments of 32 lanes x 8
+//      samples, re-reading the rows just streamed (L2 hits).
+//   C. Items fold into blocks of 32 (the warp that finishes a block sums it).
+//      Warps that find no item left take frames to walk, each waiting for its
+//      frame's last block: each plane's rows are added exactly, in closed form
+//      (binades 53 and 54, from the row's exact sum and odd count), by their
+//      run (from 55 up), or term by term where a row crosses a binade; psnr
+//      adds the exact row sums in row order (ADR-1499 "Decision"). Crossings
+//      are found by two-level warp searches over per-lane ranges. It writes
+//      the doubles the CPU divides out.
 #include <climits>
 
 #include "vmx.h"
@@ -73,6 +77,7 @@ struct Samples<uint16_t> {
     static constexpr int kPerVec = 8;
     static constexpr int kShift = 3;
     __device__ static uint32_t one(const unsigned char *row, int j) { return ld_u16(row + 2 * j); }
+    __device__ static uint64_t term(uint32_t s) { return term_of_sample(s); }
 };
 
 template <>
@@ -80,6 +85,7 @@ struct Samples<uint8_t> {
     static constexpr int kPerVec = 16;
     static constexpr int kShift = 4;
     __device__ static uint32_t one(const unsigned char *row, int j) { return ld_u8(row + j); }
+    __device__ static uint64_t term(uint32_t s) { return (uint64_t)(s * s); }
 };
 
 // Vector v of a row of `width` samples: 16 bytes, zero past the row's end.
@@ -101,7 +107,9 @@ __device__ __forceinline__ uint4 load_vec(const unsigned char *row, int v, int w
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// ------------------------------------------------------- warp reductions ---
+// ------------------------------------------------------- warp primitives ---
+
+__device__ __forceinline__ int lane_id() { return (int)(threadIdx.x & 31); }
 
 __device__ __forceinline__ uint64_t warp_sum(uint64_t v)
 {
@@ -110,58 +118,160 @@ __device__ __forceinline__ uint64_t warp_sum(uint64_t v)
     return v;
 }
 
+// A pair of running sums: the exact sum of terms and how many were odd.
+struct SC {
+    uint64_t s, c;
+};
+
+__device__ __forceinline__ SC sc_add(SC a, SC b) { return SC{a.s + b.s, a.c + b.c}; }
+
+__device__ __forceinline__ SC shfl_sc(SC x, int src)
+{
+    return SC{__shfl_sync(kFull, x.s, src), __shfl_sync(kFull, x.c, src)};
+}
+
+// Exclusive prefix of the lanes' pairs, in lane order; *total the warp total.
+__device__ __forceinline__ SC warp_excl_sc(SC x, SC *total)
+{
+    const int lane = lane_id();
+    SC v = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const SC o{__shfl_up_sync(kFull, v.s, off), __shfl_up_sync(kFull, v.c, off)};
+        if (lane >= off) v = sc_add(v, o);
+    }
+    *total = shfl_sc(v, 31);
+    return SC{v.s - x.s, v.c - x.c};
+}
+
+__device__ __forceinline__ Run shfl_run(const Run &r, int src)
+{
+    return Run{{__shfl_sync(kFull, r.inc[0], src), __shfl_sync(kFull, r.inc[1], src)}};
+}
+
+// Exclusive composition of the lanes' runs in lane order (earlier first).
+__device__ __forceinline__ Run warp_excl_run(const Run &x, int sh, Run *total)
+{
+    const int lane = lane_id();
+    Run v = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const Run o{{__shfl_up_sync(kFull, v.inc[0], off), __shfl_up_sync(kFull, v.inc[1], off)}};
+        if (lane >= off) v = compose(o, v, sh);
+    }
+    *total = shfl_run(v, 31);
+    Run ex{{__shfl_up_sync(kFull, v.inc[0], 1), __shfl_up_sync(kFull, v.inc[1], 1)}};
+    if (lane == 0) ex = run_identity();
+    return ex;
+}
+
 // --------------------------------------------------- phase A: row sums ---
 
 struct RowSums {
     uint64_t t2r, t2d, tp, s1r, s1d;
+    uint32_t oddr, oddd;
 };
 
-// Per-lane accumulators of a 16-bit row. g = 2^23 + p as bits is both the
-// binary32 2^23 + p (so f = g - 2^23 = p exactly) and an integer; sums of g^2
-// give sums of p^2 modulo 2^64 once n * kA^2 + 2 kA sum(p) is taken off.
+// Per-lane accumulators of a 16-bit row, two samples per binary32x2 lane
+// pair. g = 2^23 + p as bits is both the binary32 2^23 + p (so f = g - 2^23
+// = p exactly) and an integer: integer sums of g give sums of p (less n kA),
+// sums of g^2 give sums of p^2 modulo 2^64 once n kA^2 + 2 kA sum(p) is taken
+// off, and the binary32 square is p^2 minus its rounding error
+// e = fma(f, f, -fl(f * f)), summed exactly in binary32. psnr: with both
+// planes, sum d^2 = sum p^2 + sum q^2 - 2 sum pq, the cross term from sums of
+// g_r * g_d; alone, from the signed difference.
+// Odd terms: a binary32 square t = p^2 - e is odd exactly when p - e is.
+// Adding integers with round-toward-zero to a float whose last place is 2
+// (in [2^24, 2^25)) drops exactly 1 for each odd one, so G (the samples
+// added so) and H (the errors added so) count the odd p and the odd e, and
+// the odd terms are their difference.
 struct Acc16 {
-    float s1r, s1d, er, ed, ep;
-    uint32_t s1r_i, s1d_i, n;
-    uint64_t ggr, ggd, dd;
+    float2 er, ed, ep, gor, god, hor, hod;
+    uint32_t gsr, gsd, s1r_i, s1d_i, n, oddr, oddd;
+    int32_t er_i, ed_i;
+    uint64_t ggr, ggd, gx;
 };
 
-template <bool M, bool P>
+constexpr float kG0 = 16777216.0f;  // 2^24
+constexpr float kH0 = 25165824.0f;  // 1.5 * 2^24: room for errors of either sign
+
+__device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
+
+template <bool M, bool P, bool ODD>
 __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
 {
     const uint32_t gr0 = __byte_perm(r, kA, 0x7610), gr1 = __byte_perm(r, kA, 0x7632);
     const uint32_t gd0 = __byte_perm(d, kA, 0x7610), gd1 = __byte_perm(d, kA, 0x7632);
-    const float fr0 = __fsub_rn(__uint_as_float(gr0), 8388608.0f);
-    const float fr1 = __fsub_rn(__uint_as_float(gr1), 8388608.0f);
-    const float fd0 = __fsub_rn(__uint_as_float(gd0), 8388608.0f);
-    const float fd1 = __fsub_rn(__uint_as_float(gd1), 8388608.0f);
+    const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
+    const float2 fr = __fadd2_rn(make_float2(__uint_as_float(gr0), __uint_as_float(gr1)), m23);
+    const float2 fd = __fadd2_rn(make_float2(__uint_as_float(gd0), __uint_as_float(gd1)), m23);
     if (M) {
-        a.s1r = __fadd_rn(a.s1r, __fadd_rn(fr0, fr1));
-        a.s1d = __fadd_rn(a.s1d, __fadd_rn(fd0, fd1));
-        float t;
-        t = __fmul_rn(fr0, fr0); a.er = __fadd_rn(a.er, __fmaf_rn(fr0, fr0, -t));
-        t = __fmul_rn(fr1, fr1); a.er = __fadd_rn(a.er, __fmaf_rn(fr1, fr1, -t));
-        t = __fmul_rn(fd0, fd0); a.ed = __fadd_rn(a.ed, __fmaf_rn(fd0, fd0, -t));
-        t = __fmul_rn(fd1, fd1); a.ed = __fadd_rn(a.ed, __fmaf_rn(fd1, fd1, -t));
+        a.gsr += gr0 + gr1;
+        a.gsd += gd0 + gd1;
+        const float2 er = __ffma2_rn(fr, fr, neg2(__fmul2_rn(fr, fr)));  // exact errors
+        const float2 ed = __ffma2_rn(fd, fd, neg2(__fmul2_rn(fd, fd)));
+        a.er = __fadd2_rn(a.er, er);
+        a.ed = __fadd2_rn(a.ed, ed);
         a.ggr += (uint64_t)gr0 * gr0;
         a.ggr += (uint64_t)gr1 * gr1;
         a.ggd += (uint64_t)gd0 * gd0;
         a.ggd += (uint64_t)gd1 * gd1;
+        if (ODD) {
+            a.gor = __fadd2_rz(a.gor, fr);
+            a.god = __fadd2_rz(a.god, fd);
+            a.hor = __fadd2_rz(a.hor, er);
+            a.hod = __fadd2_rz(a.hod, ed);
+        }
     }
     if (P) {
-        const float x0 = __fsub_rn(fr0, fd0), x1 = __fsub_rn(fr1, fd1);  // exact
-        float t;
-        t = __fmul_rn(x0, x0); a.ep = __fadd_rn(a.ep, __fmaf_rn(x0, x0, -t));
-        t = __fmul_rn(x1, x1); a.ep = __fadd_rn(a.ep, __fmaf_rn(x1, x1, -t));
-        const int32_t i0 = (int32_t)(gr0 - gd0), i1 = (int32_t)(gr1 - gd1);
-        a.dd += (uint64_t)((int64_t)i0 * i0);
-        a.dd += (uint64_t)((int64_t)i1 * i1);
+        const float2 x = __fadd2_rn(fr, neg2(fd));  // exact
+        a.ep = __fadd2_rn(a.ep, __ffma2_rn(x, x, neg2(__fmul2_rn(x, x))));
+        if (M) {
+            a.gx += (uint64_t)gr0 * gd0;
+            a.gx += (uint64_t)gr1 * gd1;
+        } else {
+            const int32_t i0 = (int32_t)(gr0 - gd0), i1 = (int32_t)(gr1 - gd1);
+            a.gx += (uint64_t)((int64_t)i0 * i0);
+            a.gx += (uint64_t)((int64_t)i1 * i1);
+        }
     }
 }
 
-template <bool M, bool P, bool VEC>
-__device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, int width, int lane)
+// Moves one iteration's sums (exact small integers) to integer totals.
+// `slots` samples per plane went into this iteration's sums.
+template <bool M, bool ODD>
+__device__ __forceinline__ void acc16_flush(Acc16 &a, uint32_t slots)
 {
+    if (!M) return;
+    const uint32_t pr = a.gsr - slots * kA, pd = a.gsd - slots * kA;  // sums of p
+    const int32_t er = small_f_to_i(__fadd_rn(a.er.x, a.er.y));
+    const int32_t ed = small_f_to_i(__fadd_rn(a.ed.x, a.ed.y));
+    a.s1r_i += pr;
+    a.s1d_i += pd;
+    a.er_i += er;
+    a.ed_i += ed;
+    if (ODD) {
+        // G - G0 = sum p - (odd p); H - H0 = sum e - (odd e).
+        const int32_t gr = small_f_to_i(__fadd_rn(__fadd_rn(a.gor.x, -kG0), __fadd_rn(a.gor.y, -kG0)));
+        const int32_t gd = small_f_to_i(__fadd_rn(__fadd_rn(a.god.x, -kG0), __fadd_rn(a.god.y, -kG0)));
+        const int32_t hr = small_f_to_i(__fadd_rn(__fadd_rn(a.hor.x, -kH0), __fadd_rn(a.hor.y, -kH0)));
+        const int32_t hd = small_f_to_i(__fadd_rn(__fadd_rn(a.hod.x, -kH0), __fadd_rn(a.hod.y, -kH0)));
+        a.oddr += (uint32_t)(((int32_t)pr - gr) - (er - hr));
+        a.oddd += (uint32_t)(((int32_t)pd - gd) - (ed - hd));
+        a.gor = a.god = make_float2(kG0, kG0);
+        a.hor = a.hod = make_float2(kH0, kH0);
+    }
+    a.gsr = a.gsd = 0;
+    a.er = a.ed = make_float2(0.0f, 0.0f);
+}
+
+template <bool M, bool P, bool ODD, bool VEC>
+__device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, int width)
+{
+    const int lane = lane_id();
     Acc16 a = {};
+    a.gor = a.god = make_float2(kG0, kG0);
+    a.hor = a.hod = make_float2(kH0, kH0);
     const int nvt = (width + 7) >> 3;
     for (int base = 0; base < nvt; base += 32 * kUnroll) {
         uint4 R[kUnroll], D[kUnroll];
@@ -173,42 +283,51 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            acc16_word<M, P>(a, R[u].x, D[u].x);
-            acc16_word<M, P>(a, R[u].y, D[u].y);
-            acc16_word<M, P>(a, R[u].z, D[u].z);
-            acc16_word<M, P>(a, R[u].w, D[u].w);
+            acc16_word<M, P, ODD>(a, R[u].x, D[u].x);
+            acc16_word<M, P, ODD>(a, R[u].y, D[u].y);
+            acc16_word<M, P, ODD>(a, R[u].z, D[u].z);
+            acc16_word<M, P, ODD>(a, R[u].w, D[u].w);
         }
         a.n += 8 * kUnroll;
-        if (M) {  // move the float sums of p (below 2^23, exact) to integers
-            a.s1r_i += small_f_to_u(a.s1r);
-            a.s1d_i += small_f_to_u(a.s1d);
-            a.s1r = 0.0f;
-            a.s1d = 0.0f;
-        }
+        acc16_flush<M, ODD>(a, 8 * kUnroll);
     }
-    RowSums out = {0, 0, 0, 0, 0};
+    RowSums out = {0, 0, 0, 0, 0, 0, 0};
+    const uint64_t n = a.n;
+    const uint64_t pr = a.ggr - n * kA2 - 2ull * kA * (uint64_t)a.s1r_i;  // sum p^2
+    const uint64_t pd = a.ggd - n * kA2 - 2ull * kA * (uint64_t)a.s1d_i;
     if (M) {
-        const uint64_t n = a.n;
-        const uint64_t pr = a.ggr - n * kA2 - 2ull * kA * (uint64_t)a.s1r_i;  // sum p^2
-        const uint64_t pd = a.ggd - n * kA2 - 2ull * kA * (uint64_t)a.s1d_i;
-        out.t2r = pr - (uint64_t)(int64_t)small_f_to_i(a.er);
-        out.t2d = pd - (uint64_t)(int64_t)small_f_to_i(a.ed);
+        out.t2r = pr - (uint64_t)(int64_t)a.er_i;
+        out.t2d = pd - (uint64_t)(int64_t)a.ed_i;
         out.s1r = a.s1r_i;
         out.s1d = a.s1d_i;
     }
-    if (P) out.tp = a.dd - (uint64_t)(int64_t)small_f_to_i(a.ep);
+    if (P) {
+        uint64_t d2 = a.gx;  // sum d^2 (alone) or sum g_r g_d (with moments)
+        if (M) {
+            const uint64_t pq = a.gx - n * kA2 - (uint64_t)kA * ((uint64_t)a.s1r_i + a.s1d_i);
+            d2 = pr + pd - 2ull * pq;
+        }
+        out.tp = d2 - (uint64_t)(int64_t)small_f_to_i(__fadd_rn(a.ep.x, a.ep.y));
+    }
+    // Row totals; the first-moment sums stay per lane (the item adds them).
     out.t2r = warp_sum(out.t2r);
     out.t2d = warp_sum(out.t2d);
     out.tp = warp_sum(out.tp);
-    out.s1r = warp_sum(out.s1r);
-    out.s1d = warp_sum(out.s1d);
+    if (ODD) {  // both counts fit 16 bits (a row has at most 2^15 samples)
+        uint32_t packed = a.oddr | (a.oddd << 16);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) packed += __shfl_xor_sync(kFull, packed, off);
+        out.oddr = packed & 0xffffu;
+        out.oddd = packed >> 16;
+    }
     return out;
 }
 
 // 8-bit rows: every square is below 2^16, exact; byte dot products.
 template <bool M, bool P, bool VEC>
-__device__ RowSums row_sums8(const unsigned char *rr, const unsigned char *dr, int width, int lane)
+__device__ RowSums row_sums8(const unsigned char *rr, const unsigned char *dr, int width)
 {
+    const int lane = lane_id();
     uint32_t s1r = 0, s1d = 0, s2r = 0, s2d = 0, srd = 0;
     const int nvt = (width + 15) >> 4;
     for (int base = 0; base < nvt; base += 32 * kUnroll) {
@@ -239,20 +358,21 @@ __device__ RowSums row_sums8(const unsigned char *rr, const unsigned char *dr, i
     out.t2r = warp_sum(s2r);
     out.t2d = warp_sum(s2d);
     out.tp = P ? out.t2r + out.t2d - 2ull * warp_sum(srd) : 0ull;
-    out.s1r = warp_sum(s1r);
-    out.s1d = warp_sum(s1d);
+    out.s1r = s1r;  // per lane; the item adds them
+    out.s1d = s1d;
+    out.oddr = out.oddd = 0;
     return out;
 }
 
 // ------------------------------------------------ phase B: row runs ---
 
-// The run of row `row` (16-bit samples) under binade e: segments of 32 lanes
-// x 8 samples, each lane's 8 terms a compact run, lanes composed by an
-// order-preserving shuffle tree (lane i takes lane i + off), segments
-// composed in order.
+// The run of a 16-bit row under binade e: segments of 32 lanes x 8 samples,
+// each lane's 8 terms a compact run, lanes composed by an order-preserving
+// shuffle tree (lane i takes lane i + off), segments composed in order.
 template <bool VEC>
-__device__ Run row_run16(const unsigned char *row, int width, int e, uint64_t exact, int lane)
+__device__ __noinline__ Run row_run16(const unsigned char *row, int width, int e, uint64_t exact)
 {
+    const int lane = lane_id();
     const int sh = e - 52;
     const int nvt = (width + 7) >> 3;
     LaneRun acc = lane_identity();
@@ -291,297 +411,262 @@ __device__ Run row_run16(const unsigned char *row, int width, int e, uint64_t ex
     return lane_to_run(acc, exact);
 }
 
-// ------------------------------------------------------ shared memory ---
-
-struct Smem {
-    int ticket;
-    int last;
-    int minv[kWarps];
-    uint64_t rows[2][kMaxRowsPerTile];  // this tile's second-moment row sums
-    uint64_t wpart[kWarps][4];          // per-warp tile partials
-    uint64_t tile_tot[2];
-    uint64_t prefix[2];
-    uint64_t scan[kWarps][2];
-    uint64_t sval;
-};
-
-// ------------------------------------------------------ CTA primitives ---
-
-__device__ __forceinline__ int cta_min(int x, Smem &sm)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int m = __reduce_min_sync(kFull, x);
-    if (lane == 0) sm.minv[warp] = m;
-    __syncthreads();
-    int r = INT_MAX;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) r = min(r, sm.minv[w]);
-    __syncthreads();
-    return r;
-}
-
-// Exclusive prefix sum over threads in thread order; *total gets the sum.
-__device__ __forceinline__ uint64_t cta_excl_sum(uint64_t x, uint64_t *total, Smem &sm)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint64_t v = x;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint64_t o = __shfl_up_sync(kFull, v, off);
-        if (lane >= off) v += o;
-    }
-    if (lane == 31) sm.scan[warp][0] = v;
-    __syncthreads();
-    uint64_t pre = 0, tot = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const uint64_t s = sm.scan[w][0];
-        if (w < warp) pre += s;
-        tot += s;
-    }
-    __syncthreads();
-    *total = tot;
-    return pre + v - x;
-}
-
-__device__ __forceinline__ Run shfl_up_run(const Run &r, int off)
-{
-    Run o;
-    o.inc[0] = __shfl_up_sync(kFull, r.inc[0], off);
-    o.inc[1] = __shfl_up_sync(kFull, r.inc[1], off);
-    return o;
-}
-
-// Exclusive composition of runs in thread order (earlier runs first).
-__device__ __forceinline__ Run cta_excl_run(const Run &x, int sh, Run *total, Smem &sm)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    Run v = x;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const Run o = shfl_up_run(v, off);
-        if (lane >= off) v = compose(o, v, sh);
-    }
-    Run ex = shfl_up_run(v, 1);
-    if (lane == 0) ex = run_identity();
-    if (lane == 31) {
-        sm.scan[warp][0] = v.inc[0];
-        sm.scan[warp][1] = v.inc[1];
-    }
-    __syncthreads();
-    Run pre = run_identity(), tot = run_identity();
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const Run s = Run{{sm.scan[w][0], sm.scan[w][1]}};
-        if (w < warp) pre = compose(pre, s, sh);
-        tot = compose(tot, s, sh);
-    }
-    __syncthreads();
-    *total = tot;
-    return compose(pre, ex, sh);
-}
-
-__device__ __forceinline__ uint64_t cta_broadcast_from_owner(bool owner, uint64_t v, Smem &sm)
-{
-    if (owner) sm.sval = v;
-    __syncthreads();
-    const uint64_t r = sm.sval;
-    __syncthreads();
-    return r;
-}
-
 // ------------------------------------------------------ phase C: walk ---
 
-// Adds n terms in order to S by the CPU's rule: exact adds while the sum
-// stays at or below 2^53, the binade's runs while it stays below the next
-// power of two, and the full rounding of the one term that crosses.
-template <class Fetch>
-__device__ uint64_t cta_apply_terms(uint64_t S, int n, Fetch fetch, Smem &sm, uint32_t *ctrl)
+__device__ __forceinline__ void count(uint32_t *ctrl, int which, uint32_t n)
 {
-    constexpr int kPer = 8;
-    constexpr int kChunk = kThreads * kPer;
-    int pos = 0;
-    while (pos < n) {
-        const int q0 = pos + threadIdx.x * kPer;
-        uint64_t t[kPer];
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) t[i] = (q0 + i < n) ? fetch(q0 + i) : 0ull;
-        int bad = INT_MAX;
-        uint64_t next = 0;
-        if (threadIdx.x == 0) atomicAdd(ctrl + kCtrlTermChunks, 1u);
-        if (S < kTwo53) {
-            uint64_t a = 0;
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) a += t[i];
-            uint64_t tot;
-            uint64_t s = S + cta_excl_sum(a, &tot, sm);
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) {
-                const uint64_t x = s + t[i];
-                if (bad == INT_MAX && q0 + i < n && x > kTwo53) {
-                    bad = q0 + i;
-                    next = rnd53(x);
-                }
-                s = x;
-            }
-            const int m = cta_min(bad, sm);
-            if (m == INT_MAX) {
-                S += tot;
-                pos += kChunk;
-                continue;
-            }
-            S = cta_broadcast_from_owner(bad == m, next, sm);
-            pos = m + 1;
-        } else {
-            const int b = binade_of(S), sh = b - 52;
-            const uint64_t top = 2ull << b;
-            Run run = run_identity();
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) run = compose(run, run_of_term(t[i], sh), sh);
-            Run tot;
-            uint64_t s = apply(cta_excl_run(run, sh, &tot, sm), S, sh);
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) {
-                if (bad != INT_MAX || q0 + i >= n) continue;
-                const uint64_t x = s + t[i];
-                if (x >= top) {
-                    bad = q0 + i;
-                    next = rnd53(x);
-                } else {
-                    s = apply(run_of_term(t[i], sh), s, sh);
-                }
-            }
-            const int m = cta_min(bad, sm);
-            if (m == INT_MAX) {
-                S = apply(tot, S, sh);
-                pos += kChunk;
-                continue;
-            }
-            S = cta_broadcast_from_owner(bad == m, next, sm);
-            pos = m + 1;
+    if (lane_id() == 0 && n) atomicAdd(ctrl + which, n);
+}
+
+// Two-level search. Among the elements [lo, hi) (pairs from fetch(i)), finds
+// the first index m whose inclusive prefix (summed from lo) makes bad() true;
+// bad must be monotone along the prefix. *before gets the prefix before m
+// (the whole sum when no element is bad; then hi is returned). Each pass
+// gives every lane a contiguous range, scans the lanes' sums and narrows to
+// the range where bad() turns true, until a range of at most 4 per lane.
+template <class Fetch, class Bad>
+__device__ int warp_first(Fetch fetch, int lo, int hi, Bad bad, SC *before, uint32_t *ctrl)
+{
+    const int lane = lane_id();
+    SC base{0, 0};
+    for (;;) {
+        count(ctrl, kCtrlPasses, 1);
+        const int len = hi - lo;
+        if (len <= 0) {
+            *before = base;
+            return hi;
         }
+        const int c = (len + 31) / 32;
+        const int a = lo + lane * c;
+        const int b = min(hi, a + c);
+        if (c <= 4) {
+            SC v[4];
+            SC loc{0, 0};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[i] = (a + i < b) ? fetch(a + i) : SC{0, 0};
+                loc = sc_add(loc, v[i]);
+            }
+            SC tot;
+            SC cur = sc_add(base, warp_excl_sc(loc, &tot));
+            int cand = INT_MAX;
+            SC cb{0, 0};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (cand != INT_MAX || a + i >= b) continue;
+                const SC nx = sc_add(cur, v[i]);
+                if (bad(nx)) {
+                    cand = a + i;
+                    cb = cur;
+                }
+                cur = nx;
+            }
+            const unsigned m = __ballot_sync(kFull, cand != INT_MAX);
+            if (!m) {
+                *before = sc_add(base, tot);
+                return hi;
+            }
+            const int src = __ffs(m) - 1;
+            *before = shfl_sc(cb, src);
+            return __shfl_sync(kFull, cand, src);
+        }
+        SC loc{0, 0};
+#pragma unroll 4
+        for (int i = a; i < b; ++i) loc = sc_add(loc, fetch(i));
+        SC tot;
+        const SC ex = warp_excl_sc(loc, &tot);
+        const bool hit = a < b && bad(sc_add(base, sc_add(ex, loc)));
+        const unsigned m = __ballot_sync(kFull, hit);
+        if (!m) {
+            *before = sc_add(base, tot);
+            return hi;
+        }
+        const int src = __ffs(m) - 1;
+        base = sc_add(base, shfl_sc(ex, src));
+        const int nlo = lo + src * c;
+        hi = min(hi, nlo + c);
+        lo = nlo;
+    }
+}
+
+// Runs in order from S (S >= 2^53, binade b fixed): returns the first index m
+// in [lo, hi) whose element has no valid run or would take S to 2^(b+1) or
+// more, and leaves in S the value before m (after all, when m == hi).
+// run_at(i, sh, &ok) gives element i's run under last place 2^sh.
+template <class RunAt>
+__device__ int warp_run_walk(RunAt run_at, int lo, int hi, uint64_t &S, uint32_t *ctrl)
+{
+    const int lane = lane_id();
+    const int b = binade_of(S), sh = b - 52;
+    const uint64_t top = 2ull << b;
+    for (int c0 = lo; c0 < hi; c0 += 128) {
+        count(ctrl, kCtrlPasses, 1);
+        const int q0 = c0 + lane * 4;
+        Run r[4];
+        bool ok[4];
+        Run lr = run_identity();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ok[i] = true;
+            r[i] = run_identity();
+            if (q0 + i < hi) r[i] = run_at(q0 + i, sh, &ok[i]);
+            if (!ok[i]) r[i] = run_identity();
+            lr = compose(lr, r[i], sh);
+        }
+        Run tot;
+        uint64_t cur = apply(warp_excl_run(lr, sh, &tot), S, sh);
+        int cand = INT_MAX;
+        uint64_t cb = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (cand != INT_MAX || q0 + i >= hi) continue;
+            const uint64_t nx = apply(r[i], cur, sh);
+            if (!ok[i] || nx >= top) {
+                cand = q0 + i;
+                cb = cur;
+            } else {
+                cur = nx;
+            }
+        }
+        const unsigned m = __ballot_sync(kFull, cand != INT_MAX);
+        if (!m) {
+            S = apply(tot, S, sh);
+            continue;
+        }
+        const int src = __ffs(m) - 1;
+        S = __shfl_sync(kFull, cb, src);
+        return __shfl_sync(kFull, cand, src);
+    }
+    return hi;
+}
+
+// Adds the terms of one row (the binary32 squares of its samples) to S by
+// the CPU's rule: exact adds while the sum stays at or below 2^53, the closed
+// forms in binades 53 and 54, runs from 55 up, and the full rounding of each
+// term that crosses into the next binade.
+template <typename TS>
+__device__ uint64_t resolve_row(const unsigned char *row, int width, uint64_t S, uint32_t *ctrl,
+                               int pos = 0)
+{
+    auto term = [row](int j) -> uint64_t { return Samples<TS>::term(Samples<TS>::one(row, j)); };
+    while (pos < width) {
+        int m;
+        if (S < kTwo53) {
+            SC before;
+            m = warp_first([&](int j) { return SC{term(j), 0}; }, pos, width,
+                           [S](SC x) { return S + x.s > kTwo53; }, &before, ctrl);
+            S += before.s;
+        } else if (binade_of(S) <= 54) {
+            const int b = binade_of(S);
+            const uint64_t top = 2ull << b;
+            SC before;
+            m = warp_first(
+                [&](int j) {
+                    const uint64_t t = term(j);
+                    return SC{t, t & 1ull};
+                },
+                pos, width, [S, b, top](SC x) { return closed_form_after(S, x.s, x.c, b) >= top; },
+                &before, ctrl);
+            S = closed_form_after(S, before.s, before.c, b);
+        } else {
+            m = warp_run_walk(
+                [&](int j, int sh, bool *ok) {
+                    *ok = true;
+                    return run_of_term(term(j), sh);
+                },
+                pos, width, S, ctrl);
+        }
+        if (m < width) S = rnd53(S + term(m));
+        pos = m + 1;
     }
     return S;
 }
 
-// The CPU's second-moment sum of plane X of frame f from its row sums and
-// row runs; rows that fit no run are added term by term from the samples.
-template <typename TS>
-__device__ uint64_t cta_walk_plane(const Params &p, int f, int X, Smem &sm)
+// The CPU's second-moment sum of plane X of frame f from row r on, S the sum
+// before row r: rows added exactly, in closed form (binades 53 and 54, from
+// the row's exact sum and odd count), by their run (from 55 up), else term
+// by term from the samples. The general path; walk_plane_fast() takes the
+// common case in a few passes and falls back here.
+template <typename TS, bool FULL>
+__device__ uint64_t walk_plane_from(const Params &p, int f, int X, int r, uint64_t S)
 {
-    constexpr int kPer = 4;
-    constexpr int kChunk = kThreads * kPer;
     const int H = p.height;
-    const uint64_t *R = p.s2_rows + ((size_t)f * 2 + X) * H;
-    const RowRec *rec = p.rec + ((size_t)f * 2 + X) * H;
+    const size_t off = ((size_t)f * 2 + X) * H;
+    const uint64_t *R = p.s2_rows + off;
+    const uint32_t *O = p.odd_rows + off;
+    const RowRec *rec = p.rec + off;
     const unsigned char *plane = (X == 0 ? p.ref : p.dis) + (int64_t)f * p.pitch;
-    uint64_t S = 0;
-    int r = 0;
     while (r < H) {
-        int m = H;
-        const bool exact = S < kTwo53;
-        const int b = exact ? 0 : binade_of(S), sh = b - 52;
-        const uint64_t top = exact ? 0 : (2ull << b);
-        for (int c0 = r; c0 < H; c0 += kChunk) {
-            const int q0 = c0 + threadIdx.x * kPer;
-            uint64_t v[kPer];
-            bool ok[kPer];
-            Run rr[kPer];
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) {
-                const int q = q0 + i;
-                v[i] = q < H ? __ldcg(R + q) : 0ull;
-                ok[i] = true;
-                rr[i] = run_identity();
-                if (!exact && q < H && v[i] != 0) {
-                    const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(rec + q));
+        int m;
+        if (S < kTwo53) {
+            SC before;
+            m = warp_first([R](int i) { return SC{__ldcg(R + i), 0}; }, r, H,
+                           [S](SC x) { return S + x.s > kTwo53; }, &before, p.ctrl);
+            S += before.s;
+            count(p.ctrl, kCtrlRowsExact, (uint32_t)(m - r));
+        } else if (binade_of(S) <= 54) {
+            const int b = binade_of(S);
+            const uint64_t top = 2ull << b;
+            SC before;
+            m = warp_first([R, O](int i) { return SC{__ldcg(R + i), (uint64_t)__ldcg(O + i)}; }, r, H,
+                           [S, b, top](SC x) { return closed_form_after(S, x.s, x.c, b) >= top; },
+                           &before, p.ctrl);
+            S = closed_form_after(S, before.s, before.c, b);
+            count(p.ctrl, kCtrlRowsRun, (uint32_t)(m - r));
+        } else if (FULL) {
+            const int b = binade_of(S);
+            m = warp_run_walk(
+                [R, rec, b](int i, int sh, bool *ok) {
+                    const uint64_t rs = __ldcg(R + i);
+                    if (rs == 0) {
+                        *ok = true;
+                        return run_identity();
+                    }
+                    const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(rec + i));
                     const uint64_t inc0 = ((uint64_t)w.y << 32) | w.x;
-                    const int32_t dinc = (int32_t)w.z;
                     const int e = (int)(w.w & 0xffu), kind = (int)((w.w >> 8) & 0xffu);
-                    ok[i] = kind == kRowRun && e == b;
-                    if (ok[i]) rr[i] = Run{{inc0, inc0 + (uint64_t)(int64_t)dinc}};
-                }
-            }
-            int bad = INT_MAX;
-            uint64_t before = 0;
-            if (exact) {
-                uint64_t a = 0;
-#pragma unroll
-                for (int i = 0; i < kPer; ++i) a += v[i];
-                uint64_t tot;
-                uint64_t s = S + cta_excl_sum(a, &tot, sm);
-#pragma unroll
-                for (int i = 0; i < kPer; ++i) {
-                    if (bad != INT_MAX || q0 + i >= H) continue;
-                    if (s + v[i] > kTwo53) {
-                        bad = q0 + i;
-                        before = s;
-                    } else {
-                        s += v[i];
-                    }
-                }
-                const int mm = cta_min(bad, sm);
-                if (mm == INT_MAX) {
-                    S += tot;
-                    continue;
-                }
-                S = cta_broadcast_from_owner(bad == mm, before, sm);
-                m = mm;
-                break;
-            } else {
-                Run run = run_identity();
-#pragma unroll
-                for (int i = 0; i < kPer; ++i) run = compose(run, rr[i], sh);
-                Run tot;
-                uint64_t s = apply(cta_excl_run(run, sh, &tot, sm), S, sh);
-#pragma unroll
-                for (int i = 0; i < kPer; ++i) {
-                    if (bad != INT_MAX || q0 + i >= H) continue;
-                    const uint64_t x = apply(rr[i], s, sh);
-                    if (!ok[i] || x >= top) {
-                        bad = q0 + i;
-                        before = s;
-                    } else {
-                        s = x;
-                    }
-                }
-                const int mm = cta_min(bad, sm);
-                if (mm == INT_MAX) {
-                    S = apply(tot, S, sh);
-                    continue;
-                }
-                S = cta_broadcast_from_owner(bad == mm, before, sm);
-                m = mm;
-                break;
-            }
+                    *ok = kind == kRowRun && e == b;
+                    return Run{{inc0, inc0 + (uint64_t)(int64_t)(int32_t)w.z}};
+                },
+                r, H, S, p.ctrl);
+            count(p.ctrl, kCtrlRowsRun, (uint32_t)(m - r));
+        } else {
+            m = r;  // no runs kept (a frame this small cannot reach 2^55)
         }
-        if (threadIdx.x == 0 && m > r)
-            atomicAdd(p.ctrl + (exact ? kCtrlRowsExact : kCtrlRowsRun), (uint32_t)(m - r));
         r = m;
         if (r < H) {
-            const unsigned char *row = plane + (int64_t)r * p.stride;
-            S = cta_apply_terms(
-                S, p.width,
-                [row](int j) -> uint64_t {
-                    const uint32_t s = Samples<TS>::one(row, j);
-                    return sizeof(TS) == 2 ? (uint64_t)term_of_sample(s) : (uint64_t)(s * s);
-                },
-                sm, p.ctrl);
-            if (threadIdx.x == 0) atomicAdd(p.ctrl + kCtrlRowsTerms, 1u);
+            S = resolve_row<TS>(plane + (int64_t)r * p.stride, p.width, S, p.ctrl);
+            count(p.ctrl, kCtrlRowsTerms, 1);
             ++r;
         }
     }
     return S;
 }
 
-__device__ __forceinline__ uint64_t cta_sum_strided(const uint64_t *a, int n, int stride,
-                                                    Smem &sm)
+// The CPU's psnr noise in units: the exact row sums added in row order.
+__device__ uint64_t walk_rows(const uint64_t *rows, int H, uint32_t *ctrl)
 {
-    uint64_t s = 0;
-    for (int i = threadIdx.x; i < n; i += kThreads) s += __ldcg(a + (size_t)i * stride);
-    uint64_t tot;
-    cta_excl_sum(s, &tot, sm);
-    return tot;
+    uint64_t S = 0;
+    int r = 0;
+    while (r < H) {
+        int m;
+        if (S < kTwo53) {
+            SC before;
+            m = warp_first([rows](int i) { return SC{__ldcg(rows + i), 0}; }, r, H,
+                           [S](SC x) { return S + x.s > kTwo53; }, &before, ctrl);
+            S += before.s;
+        } else {
+            m = warp_run_walk(
+                [rows](int i, int sh, bool *ok) {
+                    *ok = true;
+                    return run_of_term(__ldcg(rows + i), sh);
+                },
+                r, H, S, ctrl);
+        }
+        if (m < H) S = rnd53(S + __ldcg(rows + m));
+        r = m + 1;
+    }
+    return S;
 }
 
 __device__ __forceinline__ double scaled_mean(uint64_t units, int shift, double n)
@@ -592,33 +677,251 @@ __device__ __forceinline__ double scaled_mean(uint64_t units, int shift, double 
     return __ddiv_rn(__dmul_rn((double)units, scale), n);
 }
 
-template <typename TS, bool M, bool P>
-__device__ void walk_frame(const Params &p, int f, Smem &sm)
+__device__ __forceinline__ Agg load_agg(const Agg *a)
 {
-    const int T = p.tiles_per_frame;
-    const double N = (double)p.width * (double)p.height;
-    if (M) {
-        for (int X = 0; X < 2; ++X) {
-            const uint64_t s1 = cta_sum_strided(p.tile_s1 + (size_t)f * T * 2 + X, T, 2, sm);
-            const uint64_t tot = cta_sum_strided(p.tile_agg + (size_t)f * T * 2 + X, T, 2, sm);
-            uint64_t s2 = tot;
-            if (tot > kTwo53) {
-                s2 = cta_walk_plane<TS>(p, f, X, sm);
-            } else if (threadIdx.x == 0) {
-                atomicAdd(p.ctrl + kCtrlRowsExact, (uint32_t)p.height);
-            }
-            if (threadIdx.x == 0) {
-                p.moments[(size_t)f * 4 + X] = scaled_mean(s1, p.k, N);
-                p.moments[(size_t)f * 4 + 2 + X] = scaled_mean(s2, 2 * p.k, N);
-                if (p.s2_sums) p.s2_sums[(size_t)f * 2 + X] = s2;
+    const uint4 *v = reinterpret_cast<const uint4 *>(a);
+    const uint4 w0 = __ldcg(v), w1 = __ldcg(v + 1), w2 = __ldcg(v + 2);
+    Agg g;
+    g.s2[0] = ((uint64_t)w0.y << 32) | w0.x;
+    g.s2[1] = ((uint64_t)w0.w << 32) | w0.z;
+    g.s1[0] = ((uint64_t)w1.y << 32) | w1.x;
+    g.s1[1] = ((uint64_t)w1.w << 32) | w1.z;
+    g.psnr = ((uint64_t)w2.y << 32) | w2.x;
+    g.odd = ((uint64_t)w2.w << 32) | w2.z;
+    g.pad[0] = g.pad[1] = 0;
+    return g;
+}
+
+__device__ __forceinline__ void store_agg(Agg *a, const Agg &g)
+{
+    uint4 *v = reinterpret_cast<uint4 *>(a);
+    __stcg(v, make_uint4((uint32_t)g.s2[0], (uint32_t)(g.s2[0] >> 32), (uint32_t)g.s2[1],
+                         (uint32_t)(g.s2[1] >> 32)));
+    __stcg(v + 1, make_uint4((uint32_t)g.s1[0], (uint32_t)(g.s1[0] >> 32), (uint32_t)g.s1[1],
+                             (uint32_t)(g.s1[1] >> 32)));
+    __stcg(v + 2, make_uint4((uint32_t)g.psnr, (uint32_t)(g.psnr >> 32), (uint32_t)g.odd,
+                             (uint32_t)(g.odd >> 32)));
+}
+
+__device__ __forceinline__ Agg agg_zero() { return Agg{{0, 0}, {0, 0}, 0, 0, {0, 0}}; }
+
+__device__ __forceinline__ Agg agg_add(const Agg &a, const Agg &b)
+{
+    return Agg{{a.s2[0] + b.s2[0], a.s2[1] + b.s2[1]},
+               {a.s1[0] + b.s1[0], a.s1[1] + b.s1[1]},
+               a.psnr + b.psnr,
+               a.odd + b.odd,
+               {0, 0}};
+}
+
+__device__ __forceinline__ Agg warp_sum_agg(Agg a)
+{
+    a.s2[0] = warp_sum(a.s2[0]);
+    a.s2[1] = warp_sum(a.s2[1]);
+    a.s1[0] = warp_sum(a.s1[0]);
+    a.s1[1] = warp_sum(a.s1[1]);
+    a.psnr = warp_sum(a.psnr);
+    a.odd = warp_sum(a.odd);
+    return a;
+}
+
+__device__ __forceinline__ SC agg_sc(const Agg &a, int X)
+{
+    return SC{a.s2[X], X ? (a.odd >> 32) : (a.odd & 0xffffffffull)};
+}
+
+// S after a run of terms with exact sum and odd count x, in the regime S is
+// in: exact adds at or below 2^53, else the closed form of binade b (53, 54).
+__device__ __forceinline__ uint64_t regime_after(uint64_t S, SC x, bool exact, int b)
+{
+    return exact ? S + x.s : closed_form_after(S, x.s, x.c, b);
+}
+
+__device__ __forceinline__ bool regime_left(uint64_t v, bool exact, int b)
+{
+    return exact ? v > kTwo53 : v >= (2ull << b);
+}
+
+// The terms of a 16-bit row starting on a 16-byte boundary, added to S from
+// term `pos` on, in rounds of 2048 terms (64 consecutive terms per lane, from
+// eight 16-byte loads). A round that keeps S at or below 2^53, or in its
+// binade by the closed form, is added at once. Otherwise the first lane
+// where that fails puts its 64 samples in shared memory, the warp scans them
+// two per lane, the first term that leaves the regime is rounded in full,
+// and the rest of the round is added from the round's sums. From binade 55
+// up the general term walk takes over.
+__device__ uint64_t resolve_row_fast(const unsigned char *row, int width, uint64_t S,
+                                     uint32_t *ctrl)
+{
+    __shared__ uint32_t words[kWarps][32];
+    const int lane = lane_id(), wid = (int)(threadIdx.x >> 5);
+    int base = 0, pos = 0;
+    while (base < width) {
+        if (S >= kTwo53 && binade_of(S) >= 55) return resolve_row<uint16_t>(row, width, S, ctrl, pos);
+        count(ctrl, kCtrlPasses, 1);
+        const int j0 = base + lane * 64;
+        uint4 V[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) V[v] = load_vec<uint16_t, true>(row, (j0 >> 3) + v, width);
+        uint64_t ls = 0, lc = 0;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            const uint32_t w4[4] = {V[v].x, V[v].y, V[v].z, V[v].w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int j = j0 + v * 8 + k;
+                const uint32_t t = term_of_sample((w4[k >> 1] >> (16 * (k & 1))) & 0xffffu);
+                if (j >= pos && j < width) {
+                    ls += t;
+                    lc += t & 1u;
+                }
             }
         }
+        SC tot;
+        const SC ex = warp_excl_sc(SC{ls, lc}, &tot);
+        const bool exact = S < kTwo53;
+        const int b = exact ? 53 : binade_of(S);
+        if (!regime_left(regime_after(S, tot, exact, b), exact, b)) {
+            S = regime_after(S, tot, exact, b);
+            base += 32 * 64;
+            pos = base;
+            continue;
+        }
+        const int src = __ffs(__ballot_sync(
+                            kFull, regime_left(regime_after(S, sc_add(ex, SC{ls, lc}), exact, b), exact, b))) -
+                        1;
+        if (lane == src) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                words[wid][4 * v] = V[v].x;
+                words[wid][4 * v + 1] = V[v].y;
+                words[wid][4 * v + 2] = V[v].z;
+                words[wid][4 * v + 3] = V[v].w;
+            }
+        }
+        __syncwarp();
+        const uint32_t w = words[wid][lane];
+        __syncwarp();
+        const int jb = base + src * 64 + 2 * lane;
+        uint64_t t0 = term_of_sample(w & 0xffffu), t1 = term_of_sample(w >> 16);
+        if (jb < pos || jb >= width) t0 = 0;
+        if (jb + 1 < pos || jb + 1 >= width) t1 = 0;
+        SC tot2;
+        const SC ex2 = warp_excl_sc(SC{t0 + t1, (t0 & 1) + (t1 & 1)}, &tot2);
+        const SC srcpre = shfl_sc(ex, src);
+        const uint64_t c0 = regime_after(S, sc_add(srcpre, ex2), exact, b);
+        const uint64_t c1 = regime_after(c0, SC{t0, t0 & 1}, exact, b);
+        const bool bad0 = regime_left(c1, exact, b);
+        const bool bad1 = !bad0 && regime_left(regime_after(c1, SC{t1, t1 & 1}, exact, b), exact, b);
+        const int src2 = __ffs(__ballot_sync(kFull, bad0 || bad1)) - 1;
+        const bool second = __shfl_sync(kFull, (int)bad1, src2);
+        const uint64_t sb = __shfl_sync(kFull, bad0 ? c0 : c1, src2);
+        const uint64_t tm = __shfl_sync(kFull, bad0 ? t0 : t1, src2);
+        const uint64_t tfirst = __shfl_sync(kFull, t0, src2);
+        const int m = base + src * 64 + 2 * src2 + (second ? 1 : 0);
+        S = rnd53(sb + tm);
+        // The round's terms after m, from its sums.
+        SC through = sc_add(srcpre, shfl_sc(ex2, src2));
+        if (second) through = sc_add(through, SC{tfirst, tfirst & 1});
+        through = sc_add(through, SC{tm, tm & 1});
+        const SC rest{tot.s - through.s, tot.c - through.c};
+        const bool exact2 = S < kTwo53;
+        const int b2 = exact2 ? 53 : binade_of(S);
+        if (b2 <= 54 && !regime_left(regime_after(S, rest, exact2, b2), exact2, b2)) {
+            S = regime_after(S, rest, exact2, b2);
+            base += 32 * 64;
+            pos = base;
+            continue;
+        }
+        pos = m + 1;  // the round crosses again: walk it from the next term
     }
-    if (P) {
-        const uint64_t *rows = p.psnr_rows + (size_t)f * p.height;
-        const uint64_t d = cta_apply_terms(
-            0ull, p.height, [rows](int i) -> uint64_t { return __ldcg(rows + i); }, sm, p.ctrl);
-        if (threadIdx.x == 0) {
+    return S;
+}
+
+// The common case of a plane past 2^53 units: the first row whose exact
+// prefix passes 2^53 is found by narrowing blocks, items and rows (one pass
+// each); that row is walked term by term; all later rows are added by one
+// closed form if the sum then stays in its binade (always so below 2^55).
+// Anything else continues on the general path.
+template <typename TS, bool VEC, bool FULL>
+__device__ uint64_t walk_plane_fast(const Params &p, int f, int X, uint64_t tot, uint64_t tot_odd)
+{
+    const int I = p.items_per_frame, NB = p.blocks_per_frame, H = p.height;
+    const Agg *blocks = p.blocks + (size_t)f * NB;
+    const Agg *items = p.items + (size_t)f * I;
+    const size_t off = ((size_t)f * 2 + X) * H;
+    const uint64_t *R = p.s2_rows + off;
+    const uint32_t *O = p.odd_rows + off;
+    const uint64_t hi_mask = X ? 32 : 0;
+    SC b0;
+    const int blk = warp_first(
+        [blocks, X, hi_mask](int i) {
+            return SC{__ldcg(&blocks[i].s2[X]), (__ldcg(&blocks[i].odd) >> hi_mask) & 0xffffffffull};
+        },
+        0, NB, [](SC x) { return x.s > kTwo53; }, &b0, p.ctrl);
+    if (blk >= NB) return tot;  // cannot happen: tot > 2^53
+    SC b1;
+    const int it = warp_first(
+        [items, X, hi_mask](int i) {
+            return SC{__ldcg(&items[i].s2[X]), (__ldcg(&items[i].odd) >> hi_mask) & 0xffffffffull};
+        },
+        blk * kBlockItems, min(I, (blk + 1) * kBlockItems),
+        [b0](SC x) { return b0.s + x.s > kTwo53; }, &b1, p.ctrl);
+    const SC pre_items = sc_add(b0, b1);
+    SC b2;
+    const int r0 = it * p.rows_per_item;
+    const int row = warp_first([R, O](int i) { return SC{__ldcg(R + i), (uint64_t)__ldcg(O + i)}; },
+                               r0, min(H, r0 + p.rows_per_item),
+                               [pre_items](SC x) { return pre_items.s + x.s > kTwo53; }, &b2, p.ctrl);
+    const SC pre = sc_add(pre_items, b2);
+    count(p.ctrl, kCtrlRowsExact, (uint32_t)row);
+    const unsigned char *plane = (X == 0 ? p.ref : p.dis) + (int64_t)f * p.pitch;
+    const unsigned char *rp = plane + (int64_t)row * p.stride;
+    uint64_t S = pre.s;
+    if (VEC && sizeof(TS) == 2) S = resolve_row_fast(rp, p.width, S, p.ctrl);
+    else S = resolve_row<TS>(rp, p.width, S, p.ctrl);
+    count(p.ctrl, kCtrlRowsTerms, 1);
+    const uint64_t rs = __ldcg(R + row), rc = __ldcg(O + row);
+    const uint64_t rest_s = tot - pre.s - rs, rest_c = tot_odd - pre.c - rc;
+    if (S >= kTwo53 && binade_of(S) <= 54) {
+        const int b = binade_of(S);
+        const uint64_t Sn = closed_form_after(S, rest_s, rest_c, b);
+        if (Sn < (2ull << b)) {
+            count(p.ctrl, kCtrlRowsRun, (uint32_t)(H - row - 1));
+            return Sn;
+        }
+    }
+    return walk_plane_from<TS, FULL>(p, f, X, row + 1, S);
+}
+
+// One part of a frame's results: part 0 and 1 the moments of ref and dis
+// (when moments are asked for), the last part the psnr noise.
+template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC>
+__device__ __noinline__ void walk_part(const Params &p, int f, int part)
+{
+    const int NB = p.blocks_per_frame;
+    const Agg *bl = p.blocks + (size_t)f * NB;
+    Agg t = agg_zero();
+#pragma unroll 4
+    for (int i = lane_id(); i < NB; i += 32) t = agg_add(t, load_agg(bl + i));
+    t = warp_sum_agg(t);
+    const double N = (double)p.width * (double)p.height;
+    const bool lead = lane_id() == 0;
+    if (M && part < 2) {
+        const int X = part;
+        uint64_t s2 = t.s2[X];
+        const uint64_t odd = X ? (t.odd >> 32) : (t.odd & 0xffffffffull);
+        if (ODD && s2 > kTwo53) s2 = walk_plane_fast<TS, VEC, FULL>(p, f, X, t.s2[X], odd);
+        else count(p.ctrl, kCtrlRowsExact, (uint32_t)p.height);
+        if (lead) {
+            p.moments[(size_t)f * 4 + X] = scaled_mean(t.s1[X], p.k, N);
+            p.moments[(size_t)f * 4 + 2 + X] = scaled_mean(s2, 2 * p.k, N);
+            if (p.s2_sums) p.s2_sums[(size_t)f * 2 + X] = s2;
+        }
+    } else if (P) {
+        const uint64_t d = t.psnr <= kTwo53 ? t.psnr
+                                            : walk_rows(p.psnr_rows + (size_t)f * p.height, p.height, p.ctrl);
+        if (lead) {
             p.mse[f] = scaled_mean(d, 2 * p.k, N);
             if (p.noise_sums) p.noise_sums[f] = d;
         }
@@ -627,31 +930,31 @@ __device__ void walk_frame(const Params &p, int f, Smem &sm)
 
 // ---------------------------------------------------------- the kernel ---
 
-// The exact second-moment sums of the frame's tiles before tile j, by a
-// decoupled look-back over flags (1: the tile's own sums are out, 2: the
-// inclusive sums are out). Called by one thread. A wait longer than
+// The exact second-moment sums of the frame's items before item j, by a
+// decoupled look-back over flags (1: the item's own sums are out, 2: the
+// inclusive sums are out). Called by one lane. A wait longer than
 // p.spin_limit polls sets the status word and gives up.
-__device__ void lookback(const Params &p, int f, int j, uint64_t aggr, uint64_t aggd,
-                         uint64_t *pre_r, uint64_t *pre_d)
+__device__ __noinline__ void lookback(const Params &p, int f, int j, uint64_t aggr, uint64_t aggd,
+                                      uint64_t *pre_r, uint64_t *pre_d)
 {
-    const size_t base = (size_t)f * p.tiles_per_frame;
+    const size_t base = (size_t)f * p.items_per_frame;
     const size_t idx = base + j;
     uint64_t pr = 0, pd = 0;
     if (j > 0) {
-        st_release(p.flags + idx, 1u);  // tile_agg was written before the fence
+        st_release(p.flags + idx, 1u);  // the item's sums were written before the fence
         int q = j - 1;
         uint32_t spins = 0;
         for (;;) {
             const uint32_t fl = ld_acquire(p.flags + base + q);
             if (fl == 2u) {
-                pr += __ldcg(p.tile_inc + (base + q) * 2);
-                pd += __ldcg(p.tile_inc + (base + q) * 2 + 1);
+                pr += __ldcg(p.item_inc + (base + q) * 2);
+                pd += __ldcg(p.item_inc + (base + q) * 2 + 1);
                 break;
             }
             if (fl == 1u) {
-                pr += __ldcg(p.tile_agg + (base + q) * 2);
-                pd += __ldcg(p.tile_agg + (base + q) * 2 + 1);
-                --q;  // tile 0 always publishes 2, so q stays >= 0
+                pr += __ldcg(&p.items[base + q].s2[0]);
+                pd += __ldcg(&p.items[base + q].s2[1]);
+                --q;  // item 0 always publishes 2, so q stays >= 0
                 continue;
             }
             if (++spins > p.spin_limit) {
@@ -661,121 +964,149 @@ __device__ void lookback(const Params &p, int f, int j, uint64_t aggr, uint64_t 
             __nanosleep(64);
         }
     }
-    __stcg(p.tile_inc + idx * 2, pr + aggr);
-    __stcg(p.tile_inc + idx * 2 + 1, pd + aggd);
+    __stcg(p.item_inc + idx * 2, pr + aggr);
+    __stcg(p.item_inc + idx * 2 + 1, pd + aggd);
     __threadfence();
     st_release(p.flags + idx, 2u);
     *pre_r = pr;
     *pre_d = pd;
 }
 
-template <typename TS, bool M, bool P, bool ORD, bool VEC>
-__global__ void __launch_bounds__(kThreads, 2) frames_kernel(Params p)
+template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
 {
-    __shared__ Smem sm;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int T = p.tiles_per_frame;
-    const int ntiles = p.frames * T;
+    const int lane = lane_id();
+    const int I = p.items_per_frame, NB = p.blocks_per_frame;
+    const int nitems = p.frames * I;
     const int H = p.height;
     for (;;) {
-        if (threadIdx.x == 0) sm.ticket = (int)atomicAdd(p.ctrl + kCtrlTicket, 1u);
-        __syncthreads();
-        const int tk = sm.ticket;
-        if (tk >= ntiles) break;
-        const int f = tk / T, j = tk - f * T;
-        const int r0 = j * p.rows_per_tile, r1 = min(H, r0 + p.rows_per_tile);
+        int tk = 0;
+        if (lane == 0) tk = (int)atomicAdd(p.ctrl + kCtrlTicket, 1u);
+        tk = __shfl_sync(kFull, tk, 0);
+        if (tk >= nitems) break;
+        const int f = tk / I, j = tk - f * I;
+        const int r0 = j * p.rows_per_item, r1 = min(H, r0 + p.rows_per_item);
         const unsigned char *fr = p.ref + (int64_t)f * p.pitch;
         const unsigned char *fd = p.dis + (int64_t)f * p.pitch;
 
         // A. exact row sums.
-        uint64_t w2r = 0, w2d = 0, w1r = 0, w1d = 0;
-        for (int r = r0 + warp; r < r1; r += kWarps) {
-            const RowSums rs = sizeof(TS) == 2
-                                   ? row_sums16<M, P, VEC>(fr + (int64_t)r * p.stride,
-                                                           fd + (int64_t)r * p.stride, p.width, lane)
-                                   : row_sums8<M, P, VEC>(fr + (int64_t)r * p.stride,
-                                                          fd + (int64_t)r * p.stride, p.width, lane);
+        Agg g = agg_zero();
+        uint64_t my_r = 0, my_d = 0;
+        for (int r = r0; r < r1; ++r) {
+            const unsigned char *rr = fr + (int64_t)r * p.stride;
+            const unsigned char *dr = fd + (int64_t)r * p.stride;
+            const RowSums rs = sizeof(TS) == 2 ? row_sums16<M, P, ODD, VEC>(rr, dr, p.width)
+                                               : row_sums8<M, P, VEC>(rr, dr, p.width);
             if (lane == 0) {
                 if (M) {
                     p.s2_rows[((size_t)f * 2) * H + r] = rs.t2r;
                     p.s2_rows[((size_t)f * 2 + 1) * H + r] = rs.t2d;
-                    sm.rows[0][r - r0] = rs.t2r;
-                    sm.rows[1][r - r0] = rs.t2d;
-                    w2r += rs.t2r;
-                    w2d += rs.t2d;
-                    w1r += rs.s1r;
-                    w1d += rs.s1d;
+                }
+                if (ODD) {
+                    p.odd_rows[((size_t)f * 2) * H + r] = rs.oddr;
+                    p.odd_rows[((size_t)f * 2 + 1) * H + r] = rs.oddd;
                 }
                 if (P) p.psnr_rows[(size_t)f * H + r] = rs.tp;
             }
+            g.s2[0] += rs.t2r;
+            g.s2[1] += rs.t2d;
+            g.s1[0] += rs.s1r;
+            g.s1[1] += rs.s1d;
+            g.psnr += rs.tp;
+            g.odd += (uint64_t)rs.oddr | ((uint64_t)rs.oddd << 32);
+            if (FULL && lane == r - r0) {
+                my_r = rs.t2r;
+                my_d = rs.t2d;
+            }
         }
-        if (M) {
+        g.s1[0] = warp_sum(g.s1[0]);
+        g.s1[1] = warp_sum(g.s1[1]);
+        if (lane == 0) store_agg(p.items + (size_t)f * I + j, g);
+
+        // B. frames that can pass 2^55: runs of the rows planned from 55 up.
+        if (FULL && M) {
+            uint64_t pr = 0, pd = 0;
             if (lane == 0) {
-                sm.wpart[warp][0] = w2r;
-                sm.wpart[warp][1] = w2d;
-                sm.wpart[warp][2] = w1r;
-                sm.wpart[warp][3] = w1d;
+                __threadfence();
+                lookback(p, f, j, g.s2[0], g.s2[1], &pr, &pd);
             }
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                uint64_t a[4] = {0, 0, 0, 0};
-                for (int w = 0; w < kWarps; ++w)
-                    for (int i = 0; i < 4; ++i) a[i] += sm.wpart[w][i];
-                const size_t idx = (size_t)f * T + j;
-                __stcg(p.tile_agg + idx * 2, a[0]);
-                __stcg(p.tile_agg + idx * 2 + 1, a[1]);
-                __stcg(p.tile_s1 + idx * 2, a[2]);
-                __stcg(p.tile_s1 + idx * 2 + 1, a[3]);
-                sm.tile_tot[0] = a[0];
-                sm.tile_tot[1] = a[1];
-                if (ORD) {
-                    __threadfence();
-                    lookback(p, f, j, a[0], a[1], &sm.prefix[0], &sm.prefix[1]);
-                }
-            }
-            __syncthreads();
-            // B. row runs of planes that are past 2^53 in this tile.
-            if (ORD) {
-                for (int X = 0; X < 2; ++X) {
-                    if (sm.prefix[X] + sm.tile_tot[X] <= kTwo53) continue;
-                    const unsigned char *plane = X == 0 ? fr : fd;
-                    for (int r = r0 + warp; r < r1; r += kWarps) {
-                        uint64_t pre = 0;
-                        for (int q = lane; q < r - r0; q += 32) pre += sm.rows[X][q];
-                        pre = warp_sum(pre) + sm.prefix[X];
-                        const uint64_t rs = sm.rows[X][r - r0];
-                        const int e = plan_binade(pre, rs);
-                        RowRec rec = {0ull, 0, 0, kRowNone, 0};
-                        if (e) {
-                            const Run run = row_run16<VEC>(plane + (int64_t)r * p.stride, p.width, e,
-                                                           rs, lane);
-                            rec.inc0 = run.inc[0];
-                            rec.dinc = (int32_t)(run.inc[1] - run.inc[0]);
-                            rec.e = (uint8_t)e;
-                            rec.kind = kRowRun;
-                        }
-                        if (lane == 0) p.rec[((size_t)f * 2 + X) * H + r] = rec;
+            pr = __shfl_sync(kFull, pr, 0);
+            pd = __shfl_sync(kFull, pd, 0);
+            for (int X = 0; X < 2; ++X) {
+                const uint64_t pre = X ? pd : pr;
+                const uint64_t mine = X ? my_d : my_r;
+                SC tot;
+                const uint64_t ex = warp_excl_sc(SC{mine, 0}, &tot).s;
+                const unsigned char *plane = X ? fd : fr;
+                for (int r = r0; r < r1; ++r) {
+                    const int li = r - r0;
+                    const uint64_t rp = pre + __shfl_sync(kFull, ex, li);
+                    const uint64_t rs = __shfl_sync(kFull, mine, li);
+                    const int e = plan_binade(rp, rs);
+                    RowRec rec = {0ull, 0, 0, kRowNone, 0};
+                    if (e >= 55) {
+                        const Run run = row_run16<VEC>(plane + (int64_t)r * p.stride, p.width, e, rs);
+                        rec.inc0 = run.inc[0];
+                        rec.dinc = (int32_t)(run.inc[1] - run.inc[0]);
+                        rec.e = (uint8_t)e;
+                        rec.kind = kRowRun;
                     }
+                    if (lane == 0) p.rec[((size_t)f * 2 + X) * H + r] = rec;
                 }
             }
         }
-        // C. completion; the last tile of the frame walks it.
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uint32_t old = atomicAdd(p.done + f, 1u);
-            sm.last = old == (uint32_t)(T - 1);
-        }
-        __syncthreads();
-        if (sm.last) {
+
+        // C. completion: the warp that finishes a block of items folds it;
+        // the warp that folds a frame's last block walks the frame.
+        const int blk = j / kBlockItems;
+        int last = 0;
+        if (lane == 0) {
             __threadfence();
-            walk_frame<TS, M, P>(p, f, sm);
+            const uint32_t n = (uint32_t)min(kBlockItems, I - blk * kBlockItems);
+            last = atomicAdd(p.block_done + (size_t)f * NB + blk, 1u) + 1 == n;
         }
-        __syncthreads();
+        if (__shfl_sync(kFull, last, 0)) {
+            __threadfence();
+            const int i = blk * kBlockItems + lane;
+            Agg a = i < I ? load_agg(p.items + (size_t)f * I + i) : agg_zero();
+            a = warp_sum_agg(a);
+            if (lane == 0) {
+                store_agg(p.blocks + (size_t)f * NB + blk, a);
+                __threadfence();
+                atomicAdd(p.done + f, 1u);
+            }
+        }
+    }
+
+    // D. Walks. A warp out of items takes a part of a frame to walk (the ref
+    // moments, the dis moments, the psnr noise); it waits (bounded) until
+    // the frame's blocks are all folded: those are held by warps that are
+    // running and wait on nothing here.
+    constexpr int kParts = (M ? 2 : 0) + (P ? 1 : 0);
+    for (;;) {
+        int wt = 0;
+        if (lane == 0) wt = (int)atomicAdd(p.ctrl + kCtrlWalkTicket, 1u);
+        wt = __shfl_sync(kFull, wt, 0);
+        if (wt >= p.frames * kParts) break;
+        const int wf = wt / kParts, part = wt - wf * kParts;
+        if (lane == 0) {
+            uint32_t spins = 0;
+            while (ld_acquire(p.done + wf) < (uint32_t)NB) {
+                if (++spins > p.spin_limit) {
+                    atomicOr(p.status, 1u);
+                    break;
+                }
+                __nanosleep(128);
+            }
+            __threadfence();
+        }
+        __syncwarp();
+        __threadfence();
+        walk_part<TS, M, P, ODD, FULL, VEC>(p, wf, M ? part : 2);
     }
 }
 
-template <typename TS, bool M, bool P, bool ORD, bool VEC>
+template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC>
 cudaError_t launch_one(const Params &p, const Layout &L, cudaStream_t stream)
 {
     static int blocks_per_sm[64] = {0};  // per device ordinal, filled once
@@ -785,33 +1116,34 @@ cudaError_t launch_one(const Params &p, const Layout &L, cudaStream_t stream)
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (blocks_per_sm[dev] == 0) {
         int n = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, frames_kernel<TS, M, P, ORD, VEC>,
-                                                            kThreads, 0);
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, frames_kernel<TS, M, P, ODD, FULL, VEC>, kThreads, 0);
         if (err != cudaSuccess) return err;
         blocks_per_sm[dev] = n > 0 ? n : 1;
     }
     int sms = 0;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    const long long tiles = (long long)L.frames * L.tiles_per_frame;
-    const int grid = (int)std::min<long long>(tiles, (long long)sms * blocks_per_sm[dev]);
-    frames_kernel<TS, M, P, ORD, VEC><<<grid, kThreads, 0, stream>>>(p);
+    const long long warps = (long long)L.frames * L.items_per_frame;
+    const long long blocks = (warps + kWarps - 1) / kWarps;
+    const int grid = (int)std::min<long long>(blocks, (long long)sms * blocks_per_sm[dev]);
+    frames_kernel<TS, M, P, ODD, FULL, VEC><<<grid, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
-template <typename TS, bool M, bool P, bool ORD>
+template <typename TS, bool M, bool P, bool ODD, bool FULL>
 cudaError_t launch_vec(const Params &p, const Layout &L, bool vec, cudaStream_t s)
 {
-    return vec ? launch_one<TS, M, P, ORD, true>(p, L, s) : launch_one<TS, M, P, ORD, false>(p, L, s);
+    return vec ? launch_one<TS, M, P, ODD, FULL, true>(p, L, s)
+               : launch_one<TS, M, P, ODD, FULL, false>(p, L, s);
 }
 
-template <typename TS, bool ORD>
-cudaError_t launch_feat(const Params &p, const Layout &L, int features, bool vec, cudaStream_t s)
+template <bool M, bool P>
+cudaError_t launch_u16(const Params &p, const Layout &L, bool vec, cudaStream_t s)
 {
-    const bool m = features & VMX_FEATURE_MOMENT, ps = features & VMX_FEATURE_PSNR;
-    if (m && ps) return launch_vec<TS, true, true, ORD>(p, L, vec, s);
-    if (m) return launch_vec<TS, true, false, ORD>(p, L, vec, s);
-    return launch_vec<TS, false, true, false>(p, L, vec, s);
+    if (L.full) return launch_vec<uint16_t, M, P, true, true>(p, L, vec, s);
+    if (L.ordered) return launch_vec<uint16_t, M, P, true, false>(p, L, vec, s);
+    return launch_vec<uint16_t, M, P, false, false>(p, L, vec, s);
 }
 
 }  // namespace
@@ -819,9 +1151,15 @@ cudaError_t launch_feat(const Params &p, const Layout &L, int features, bool vec
 cudaError_t launch_frames(const Params &p, const Layout &L, int features, bool vec,
                           cudaStream_t stream)
 {
-    if (L.bpc == 8) return launch_feat<uint8_t, false>(p, L, features, vec, stream);
-    if (L.ordered) return launch_feat<uint16_t, true>(p, L, features, vec, stream);
-    return launch_feat<uint16_t, false>(p, L, features, vec, stream);
+    const bool m = features & VMX_FEATURE_MOMENT, ps = features & VMX_FEATURE_PSNR;
+    if (L.bpc == 8) {
+        if (m && ps) return launch_vec<uint8_t, true, true, false, false>(p, L, vec, stream);
+        if (m) return launch_vec<uint8_t, true, false, false, false>(p, L, vec, stream);
+        return launch_vec<uint8_t, false, true, false, false>(p, L, vec, stream);
+    }
+    if (m && ps) return launch_u16<true, true>(p, L, vec, stream);
+    if (m) return launch_u16<true, false>(p, L, vec, stream);
+    return launch_vec<uint16_t, false, true, false, false>(p, L, vec, stream);
 }
 
 }  // namespace vmx

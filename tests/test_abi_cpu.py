@@ -52,11 +52,14 @@ def test_workspace_rejects_bad_shapes(lib, args):
 def test_workspace_sizes(lib):
     small = lib.vmx_workspace_bytes(320, 240, 8, 1, 3)
     assert small > 0 and small % 256 == 0
-    # Frames above 2^21 pixels with second moments carry per-row records.
+    # Frames above 2^21 pixels with second moments keep per-row sums and odd
+    # counts; above 2^23 pixels also per-row runs.
     a = lib.vmx_workspace_bytes(3840, 2160, 16, 16, 3)
     b = lib.vmx_workspace_bytes(3840, 2160, 16, 16, 2)
-    assert a > b + 16 * 2 * 2160 * 16
+    assert a >= b + 16 * 2 * 2160 * (8 + 4)
     assert lib.vmx_workspace_bytes(3840, 2160, 16, 32, 3) > a
+    big = lib.vmx_workspace_bytes(7680, 4320, 16, 1, 3)
+    assert big >= 2 * 4320 * (8 + 4 + 16)
 
 
 def test_argument_errors_launch_nothing(lib):
