@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "vmx.h"
 #include "vmx_internal.h"
@@ -190,6 +191,7 @@ const char *vmx_strerror(int status)
     case VMX_ENOMEM: return "out of device memory";
     case VMX_ECUDA: return g_last_cuda[0] ? g_last_cuda : "CUDA error";
     case VMX_ETIMEOUT: return "a bounded device wait gave up";
+    case VMX_ESCRATCH: return "shape needs more scratch than the no-alloc call holds";
     default: return "unknown status";
     }
 }
@@ -450,4 +452,53 @@ int vmx_frames_host(const void *ref, const void *dis, int width, int height,
     return status;
 }
 
+// The no-alloc call's scratch address per device, looked up on the first
+// call made with that device current.
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<void *> g_noalloc_ptr[kMaxDevices];
+std::mutex g_noalloc_mu;
+}  // namespace
+
+int vmx_frames_noalloc(const void *ref, const void *dis, int width, int height,
+                       int64_t stride_bytes, int bpc, int nframes, int features,
+                       double *moments, uint64_t *s2_rows, uint64_t *s2_sums,
+                       uint64_t *psnr_rows, double *mse, uint64_t *noise_sums,
+                       uint32_t *status, void *stream)
+{
+    // Shape checks first: nothing touches the device for a rejected shape.
+    Layout L;
+    if (!make_layout(width, height, bpc, nframes, features, &L)) return VMX_EINVAL;
+    if (L.total > VMX_NOALLOC_SCRATCH_BYTES) return VMX_ESCRATCH;
+    int dev = -1;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return cuda_fail(err);
+    if (dev < 0 || dev >= kMaxDevices) return VMX_EINVAL;
+    void *ws = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (!ws) {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        ws = g_noalloc_ptr[dev].load(std::memory_order_relaxed);
+        if (!ws) {
+            err = noalloc_scratch_address(&ws);
+            if (err != cudaSuccess) return cuda_fail(err);
+            if (!ws) return cuda_fail(cudaErrorInvalidSymbol);
+            g_noalloc_ptr[dev].store(ws, std::memory_order_release);
+        }
+    }
+    const Outputs o{moments, s2_rows, s2_sums, psnr_rows, mse, noise_sums};
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // run_frames clears the control words (tickets, counters, the status
+    // word) on `cs` before its launch; the rest of the scratch is written
+    // before it is read.
+    const int rc = run_frames(ref, dis, width, height, stride_bytes, bpc, nframes, features, o,
+                              ws, VMX_NOALLOC_SCRATCH_BYTES, cs);
+    if (rc != VMX_OK || !status) return rc;
+    const uint32_t *dev_status =
+        reinterpret_cast<const uint32_t *>(static_cast<unsigned char *>(ws) + L.off_ctrl) +
+        kCtrlStatus;
+    err = cudaMemcpyAsync(status, dev_status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, cs);
+    return err == cudaSuccess ? VMX_OK : cuda_fail(err);
+}
+
 }  // extern "C"
+

@@ -93,4 +93,8 @@ struct Params {
 cudaError_t launch_frames(const Params &p, const Layout &L, int features, bool vec,
                           cudaStream_t stream);
 
+// Device address of the current device's static scratch array of
+// VMX_NOALLOC_SCRATCH_BYTES bytes (cudaGetSymbolAddress; no allocation).
+cudaError_t noalloc_scratch_address(void **ptr);
+
 }  // namespace vmx

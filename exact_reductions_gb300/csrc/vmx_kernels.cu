@@ -1162,4 +1162,13 @@ cudaError_t launch_frames(const Params &p, const Layout &L, int features, bool v
     return launch_vec<uint16_t, false, true, false, false>(p, L, vec, stream);
 }
 
+// Scratch of vmx_frames_noalloc: a fixed array in the module's static device
+// memory, one per device, 256-byte aligned like a caller's workspace.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[VMX_NOALLOC_SCRATCH_BYTES];
+
+cudaError_t noalloc_scratch_address(void **ptr)
+{
+    return cudaGetSymbolAddress(ptr, g_noalloc_scratch);
+}
+
 }  // namespace vmx

@@ -54,6 +54,7 @@ extern "C" {
 #define VMX_ENOMEM (-2)    /* the library could not allocate device memory */
 #define VMX_ECUDA (-3)     /* a CUDA call failed; vmx_strerror() names it */
 #define VMX_ETIMEOUT (-4)  /* a bounded device wait gave up; outputs are not valid */
+#define VMX_ESCRATCH (-5)  /* the shape needs more than VMX_NOALLOC_SCRATCH_BYTES */
 
 #define VMX_FEATURE_MOMENT 1 /* float_moment: 4 doubles per frame */
 #define VMX_FEATURE_PSNR 2   /* float_psnr: row sums and the MSE per frame */
@@ -160,6 +161,45 @@ int vmx_frames_host(const void *ref, const void *dis, int width, int height,
 void vmx_frames_host_traffic(int width, int height, int64_t stride_bytes, int bpc,
                              int nframes, int features, int want_s2_rows,
                              uint64_t *h2d_bytes, uint64_t *d2h_bytes);
+
+/*
+ * Both features (or either) with no allocation at all. The pages have no
+ * counterpart to this call: it exists for callers that cannot allocate
+ * device memory while they run, e.g. a stage whose process has handed the
+ * whole device to another framework's memory pool, or a real-time pipeline
+ * that must not call cudaMalloc/cudaFree (which can synchronise the device).
+ *
+ * Its scratch is one fixed array of VMX_NOALLOC_SCRATCH_BYTES in the
+ * library's static device memory, one per device (present whether or not
+ * this call is used). Shapes whose vmx_workspace_bytes(width, height, bpc,
+ * nframes, features) exceeds that are rejected with VMX_ESCRATCH before
+ * anything is enqueued; split the batch into fewer frames.
+ *
+ * Set-up: the first call on each device (that device current) looks up the
+ * array's address with cudaGetSymbolAddress, which may load the library's
+ * device code; make that first call before any stream capture begins. Later
+ * calls on the device only enqueue work.
+ *
+ * Each call clears the control words the kernel needs at zero (a memset on
+ * `stream`), then launches the same frame kernel as vmx_moment_psnr_frames.
+ * Overlapping calls on one device share the one scratch array and RACE:
+ * issue them on one stream, or order them with events, from one thread at
+ * a time.
+ *   features    VMX_FEATURE_* bits; outputs of a feature not asked for may
+ *               be NULL, and s2_rows, s2_sums, noise_sums may be NULL.
+ *   outputs     device pointers, layout as vmx_moment_psnr_frames().
+ *   status      device or NULL, one uint32: set on `stream` after the
+ *               kernel to 0, or to 1 when a bounded device wait gave up (the
+ *               outputs are then not valid).
+ * Asynchronous on `stream`. Returns VMX_OK, VMX_EINVAL (arguments, as the
+ * other calls), VMX_ESCRATCH, or VMX_ECUDA.
+ */
+#define VMX_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int vmx_frames_noalloc(const void *ref, const void *dis, int width, int height,
+                       int64_t stride_bytes, int bpc, int nframes, int features,
+                       double *moments, uint64_t *s2_rows, uint64_t *s2_sums,
+                       uint64_t *psnr_rows, double *mse, uint64_t *noise_sums,
+                       uint32_t *status, void *stream);
 
 /* Name of a status code (and the last CUDA error for VMX_ECUDA). */
 const char *vmx_strerror(int status);
