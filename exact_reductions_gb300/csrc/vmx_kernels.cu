@@ -36,7 +36,6 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kA = 0x4B000000u;                   // bits of 2^23 (g = kA + p)
-constexpr uint64_t kA2 = (uint64_t)kA * (uint64_t)kA;  // kA^2
 
 // ---------------------------------------------------------------- loads ---
 
@@ -172,28 +171,30 @@ struct RowSums {
     uint32_t oddr, oddd;
 };
 
-// Per-lane accumulators of a 16-bit row, two samples per binary32x2 lane
-// pair. g = 2^23 + p as bits is both the binary32 2^23 + p (so f = g - 2^23
-// = p exactly) and an integer: integer sums of g give sums of p (less n kA),
-// sums of g^2 give sums of p^2 modulo 2^64 once n kA^2 + 2 kA sum(p) is taken
-// off, and the binary32 square is p^2 minus its rounding error
-// e = fma(f, f, -fl(f * f)), summed exactly in binary32. psnr: with both
-// planes, sum d^2 = sum p^2 + sum q^2 - 2 sum pq, the cross term from sums of
-// g_r * g_d; alone, from the signed difference.
-// Odd terms: a binary32 square t = p^2 - e is odd exactly when p - e is.
-// Adding integers with round-toward-zero to a float whose last place is 2
-// (in [2^24, 2^25)) drops exactly 1 for each odd one, so G (the samples
-// added so) and H (the errors added so) count the odd p and the odd e, and
-// the odd terms are their difference.
+// Per-lane accumulators of a 16-bit row. A 32-bit word holds two samples.
+//
+// Sums of squares: with p = 256 h + l (bytes h, l), p^2 = 256 p h + p l, and
+// the two-way 16x8-bit dot products (dp2a) of a word with its own bytes
+// rearranged as [l0, l1, h0, h1] give p0 l0 + p1 l1 and p0 h0 + p1 h1 in
+// 32-bit accumulators; with the other plane's bytes they give the cross sums
+// p q of float_psnr's sum d^2 = sum p^2 + sum q^2 - 2 sum p q.
+// The binary32 square is p^2 minus its rounding error e = fma(f, f, -fl(f f)),
+// with f = p exact in binary32 (g = 2^23 + p as bits, less 2^23); the errors
+// are integers of at most 2^7 and add exactly in binary32.
+// Odd terms: a binary32 square of a codeword is odd exactly when the codeword
+// is odd and below 4096, i.e. its low byte is odd and its high byte below 16;
+// four samples (two per plane) are tested at once in byte lanes.
+// First moments: integer sums of g, less the 2^23 bias.
 struct Acc16 {
-    float2 er, ed, ep, gor, god, hor, hod;
-    uint32_t gsr, gsd, s1r_i, s1d_i, n, oddr, oddd;
-    int32_t er_i, ed_i;
-    uint64_t ggr, ggd, gx;
+    uint32_t lr, hr, ld, hd, lx, hx;  // dot-product sums since the last flush
+    uint32_t gsr, gsd;                // sums of g since the last flush
+    uint32_t oddb;                    // odd terms since the last flush, one byte per sample slot
+    float2 er, ed, ep;                // rounding errors since the last flush
+    uint64_t p2r, p2d, px;            // row sums of p^2, q^2, p q
+    uint32_t s1r, s1d, odd;           // row sums of p, q; odd terms (ref low half, dis high)
+    int32_t eri, edi, epi;            // row sums of the rounding errors
+    uint64_t dd;                      // psnr alone: row sum of d^2
 };
-
-constexpr float kG0 = 16777216.0f;  // 2^24
-constexpr float kH0 = 25165824.0f;  // 1.5 * 2^24: room for errors of either sign
 
 __device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
 
@@ -206,72 +207,72 @@ __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
     const float2 fr = __fadd2_rn(make_float2(__uint_as_float(gr0), __uint_as_float(gr1)), m23);
     const float2 fd = __fadd2_rn(make_float2(__uint_as_float(gd0), __uint_as_float(gd1)), m23);
     if (M) {
+        const uint32_t xr = __byte_perm(r, 0, 0x3120), xd = __byte_perm(d, 0, 0x3120);
+        a.lr = __dp2a_lo(r, xr, a.lr);
+        a.hr = __dp2a_hi(r, xr, a.hr);
+        a.ld = __dp2a_lo(d, xd, a.ld);
+        a.hd = __dp2a_hi(d, xd, a.hd);
+        if (P) {
+            a.lx = __dp2a_lo(r, xd, a.lx);
+            a.hx = __dp2a_hi(r, xd, a.hx);
+        }
         a.gsr += gr0 + gr1;
         a.gsd += gd0 + gd1;
-        const float2 er = __ffma2_rn(fr, fr, neg2(__fmul2_rn(fr, fr)));  // exact errors
-        const float2 ed = __ffma2_rn(fd, fd, neg2(__fmul2_rn(fd, fd)));
-        a.er = __fadd2_rn(a.er, er);
-        a.ed = __fadd2_rn(a.ed, ed);
-        a.ggr += (uint64_t)gr0 * gr0;
-        a.ggr += (uint64_t)gr1 * gr1;
-        a.ggd += (uint64_t)gd0 * gd0;
-        a.ggd += (uint64_t)gd1 * gd1;
+        a.er = __fadd2_rn(a.er, __ffma2_rn(fr, fr, neg2(__fmul2_rn(fr, fr))));
+        a.ed = __fadd2_rn(a.ed, __ffma2_rn(fd, fd, neg2(__fmul2_rn(fd, fd))));
         if (ODD) {
-            a.gor = __fadd2_rz(a.gor, fr);
-            a.god = __fadd2_rz(a.god, fd);
-            a.hor = __fadd2_rz(a.hor, er);
-            a.hod = __fadd2_rz(a.hod, ed);
+            const uint32_t lo = __byte_perm(r, d, 0x6420), hi = __byte_perm(r, d, 0x7531);
+            const uint32_t big = ((hi & 0x7F7F7F7Fu) + 0x70707070u) | hi;  // bit 7: byte >= 16
+            a.oddb += lo & ~(big >> 7) & 0x01010101u;
         }
     }
     if (P) {
         const float2 x = __fadd2_rn(fr, neg2(fd));  // exact
         a.ep = __fadd2_rn(a.ep, __ffma2_rn(x, x, neg2(__fmul2_rn(x, x))));
-        if (M) {
-            a.gx += (uint64_t)gr0 * gd0;
-            a.gx += (uint64_t)gr1 * gd1;
-        } else {
+        if (!M) {
             const int32_t i0 = (int32_t)(gr0 - gd0), i1 = (int32_t)(gr1 - gd1);
-            a.gx += (uint64_t)((int64_t)i0 * i0);
-            a.gx += (uint64_t)((int64_t)i1 * i1);
+            a.dd += (uint64_t)((int64_t)i0 * i0);
+            a.dd += (uint64_t)((int64_t)i1 * i1);
         }
     }
 }
 
-// Moves one iteration's sums (exact small integers) to integer totals.
-// `slots` samples per plane went into this iteration's sums.
-template <bool M, bool ODD>
+// Moves one iteration's sums to the row sums. `slots` samples per plane went
+// into them: at most 32 per lane keeps every 32-bit sum below 2^30 and every
+// odd-term byte below 2^8.
+template <bool M, bool P, bool ODD>
 __device__ __forceinline__ void acc16_flush(Acc16 &a, uint32_t slots)
 {
-    if (!M) return;
-    const uint32_t pr = a.gsr - slots * kA, pd = a.gsd - slots * kA;  // sums of p
-    const int32_t er = small_f_to_i(__fadd_rn(a.er.x, a.er.y));
-    const int32_t ed = small_f_to_i(__fadd_rn(a.ed.x, a.ed.y));
-    a.s1r_i += pr;
-    a.s1d_i += pd;
-    a.er_i += er;
-    a.ed_i += ed;
-    if (ODD) {
-        // G - G0 = sum p - (odd p); H - H0 = sum e - (odd e).
-        const int32_t gr = small_f_to_i(__fadd_rn(__fadd_rn(a.gor.x, -kG0), __fadd_rn(a.gor.y, -kG0)));
-        const int32_t gd = small_f_to_i(__fadd_rn(__fadd_rn(a.god.x, -kG0), __fadd_rn(a.god.y, -kG0)));
-        const int32_t hr = small_f_to_i(__fadd_rn(__fadd_rn(a.hor.x, -kH0), __fadd_rn(a.hor.y, -kH0)));
-        const int32_t hd = small_f_to_i(__fadd_rn(__fadd_rn(a.hod.x, -kH0), __fadd_rn(a.hod.y, -kH0)));
-        a.oddr += (uint32_t)(((int32_t)pr - gr) - (er - hr));
-        a.oddd += (uint32_t)(((int32_t)pd - gd) - (ed - hd));
-        a.gor = a.god = make_float2(kG0, kG0);
-        a.hor = a.hod = make_float2(kH0, kH0);
+    if (M) {
+        a.s1r += a.gsr - slots * kA;
+        a.s1d += a.gsd - slots * kA;
+        a.p2r += ((uint64_t)a.hr << 8) + a.lr;
+        a.p2d += ((uint64_t)a.hd << 8) + a.ld;
+        a.eri += small_f_to_i(__fadd_rn(a.er.x, a.er.y));
+        a.edi += small_f_to_i(__fadd_rn(a.ed.x, a.ed.y));
+        a.lr = a.hr = a.ld = a.hd = a.gsr = a.gsd = 0;
+        a.er = a.ed = make_float2(0.0f, 0.0f);
+        if (P) {
+            a.px += ((uint64_t)a.hx << 8) + a.lx;
+            a.lx = a.hx = 0;
+        }
+        if (ODD) {
+            a.odd += (a.oddb & 0x00FF00FFu) + ((a.oddb >> 8) & 0x00FF00FFu);
+            a.oddb = 0;
+        }
     }
-    a.gsr = a.gsd = 0;
-    a.er = a.ed = make_float2(0.0f, 0.0f);
+    if (P) {
+        a.epi += small_f_to_i(__fadd_rn(a.ep.x, a.ep.y));
+        a.ep = make_float2(0.0f, 0.0f);
+    }
 }
 
 template <bool M, bool P, bool ODD, bool VEC>
 __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, int width)
 {
+    static_assert(kUnroll * 8 <= 32, "flush before 32 samples per lane");
     const int lane = lane_id();
     Acc16 a = {};
-    a.gor = a.god = make_float2(kG0, kG0);
-    a.hor = a.hod = make_float2(kH0, kH0);
     const int nvt = (width + 7) >> 3;
     for (int base = 0; base < nvt; base += 32 * kUnroll) {
         uint4 R[kUnroll], D[kUnroll];
@@ -288,33 +289,25 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
             acc16_word<M, P, ODD>(a, R[u].z, D[u].z);
             acc16_word<M, P, ODD>(a, R[u].w, D[u].w);
         }
-        a.n += 8 * kUnroll;
-        acc16_flush<M, ODD>(a, 8 * kUnroll);
+        acc16_flush<M, P, ODD>(a, 8 * kUnroll);
     }
     RowSums out = {0, 0, 0, 0, 0, 0, 0};
-    const uint64_t n = a.n;
-    const uint64_t pr = a.ggr - n * kA2 - 2ull * kA * (uint64_t)a.s1r_i;  // sum p^2
-    const uint64_t pd = a.ggd - n * kA2 - 2ull * kA * (uint64_t)a.s1d_i;
     if (M) {
-        out.t2r = pr - (uint64_t)(int64_t)a.er_i;
-        out.t2d = pd - (uint64_t)(int64_t)a.ed_i;
-        out.s1r = a.s1r_i;
-        out.s1d = a.s1d_i;
+        out.t2r = a.p2r - (uint64_t)(int64_t)a.eri;
+        out.t2d = a.p2d - (uint64_t)(int64_t)a.edi;
+        out.s1r = a.s1r;
+        out.s1d = a.s1d;
     }
     if (P) {
-        uint64_t d2 = a.gx;  // sum d^2 (alone) or sum g_r g_d (with moments)
-        if (M) {
-            const uint64_t pq = a.gx - n * kA2 - (uint64_t)kA * ((uint64_t)a.s1r_i + a.s1d_i);
-            d2 = pr + pd - 2ull * pq;
-        }
-        out.tp = d2 - (uint64_t)(int64_t)small_f_to_i(__fadd_rn(a.ep.x, a.ep.y));
+        const uint64_t d2 = M ? a.p2r + a.p2d - 2ull * a.px : a.dd;  // sum d^2
+        out.tp = d2 - (uint64_t)(int64_t)a.epi;
     }
     // Row totals; the first-moment sums stay per lane (the item adds them).
     out.t2r = warp_sum(out.t2r);
     out.t2d = warp_sum(out.t2d);
     out.tp = warp_sum(out.tp);
     if (ODD) {  // both counts fit 16 bits (a row has at most 2^15 samples)
-        uint32_t packed = a.oddr | (a.oddd << 16);
+        uint32_t packed = a.odd;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) packed += __shfl_xor_sync(kFull, packed, off);
         out.oddr = packed & 0xffffu;
@@ -989,9 +982,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         const unsigned char *fr = p.ref + (int64_t)f * p.pitch;
         const unsigned char *fd = p.dis + (int64_t)f * p.pitch;
 
-        // A. exact row sums.
-        Agg g = agg_zero();
-        uint64_t my_r = 0, my_d = 0;
+        // A. exact row sums. Lane 0 records each row; the item's sums are
+        // then read back from those records, one lane per row, so that no
+        // item totals stay live across the rows.
+        uint32_t s1r = 0, s1d = 0;  // this lane's first-moment sums
         for (int r = r0; r < r1; ++r) {
             const unsigned char *rr = fr + (int64_t)r * p.stride;
             const unsigned char *dr = fd + (int64_t)r * p.stride;
@@ -1008,19 +1002,31 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
                 }
                 if (P) p.psnr_rows[(size_t)f * H + r] = rs.tp;
             }
-            g.s2[0] += rs.t2r;
-            g.s2[1] += rs.t2d;
-            g.s1[0] += rs.s1r;
-            g.s1[1] += rs.s1d;
-            g.psnr += rs.tp;
-            g.odd += (uint64_t)rs.oddr | ((uint64_t)rs.oddd << 32);
-            if (FULL && lane == r - r0) {
-                my_r = rs.t2r;
-                my_d = rs.t2d;
-            }
+            s1r += (uint32_t)rs.s1r;
+            s1d += (uint32_t)rs.s1d;
         }
-        g.s1[0] = warp_sum(g.s1[0]);
-        g.s1[1] = warp_sum(g.s1[1]);
+        __syncwarp();
+        Agg g = agg_zero();
+        uint64_t my_r = 0, my_d = 0, my_p = 0, my_o = 0;  // this lane's row (lane < rows)
+        if (lane < r1 - r0) {
+            const int r = r0 + lane;
+            if (M) {
+                my_r = __ldcg(p.s2_rows + ((size_t)f * 2) * H + r);
+                my_d = __ldcg(p.s2_rows + ((size_t)f * 2 + 1) * H + r);
+            }
+            if (ODD)
+                my_o = (uint64_t)__ldcg(p.odd_rows + ((size_t)f * 2) * H + r) |
+                       ((uint64_t)__ldcg(p.odd_rows + ((size_t)f * 2 + 1) * H + r) << 32);
+            if (P) my_p = __ldcg(p.psnr_rows + (size_t)f * H + r);
+        }
+        if (M) {
+            g.s2[0] = warp_sum(my_r);
+            g.s2[1] = warp_sum(my_d);
+            g.s1[0] = warp_sum((uint64_t)s1r);
+            g.s1[1] = warp_sum((uint64_t)s1d);
+        }
+        if (ODD) g.odd = warp_sum(my_o);
+        if (P) g.psnr = warp_sum(my_p);
         if (lane == 0) store_agg(p.items + (size_t)f * I + j, g);
 
         // B. frames that can pass 2^55: runs of the rows planned from 55 up.
