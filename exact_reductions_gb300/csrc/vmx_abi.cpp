@@ -69,12 +69,12 @@ bool make_layout(int width, int height, int bpc, int frames, int features, Layou
     L->full = L->ordered && n > ((int64_t)1 << 23);
     size_t off = 0;
     L->off_ctrl = off;
-    L->ctrl_bytes = (kCtrlWords + F + F * B + (L->full ? F * I : 0)) * sizeof(uint32_t);
-    off = align256(off + L->ctrl_bytes);
-    L->off_items = off;
-    off = align256(off + F * I * sizeof(Agg));
+    off = align256(off + (kCtrlWords + (L->full ? F * I : 0)) * sizeof(uint32_t));
     L->off_blocks = off;
     off = align256(off + F * B * sizeof(Agg));
+    L->ctrl_bytes = off;
+    L->off_items = off;
+    off = align256(off + F * I * sizeof(Agg));
     L->off_item_inc = off;
     if (L->full) off = align256(off + F * I * 2 * sizeof(uint64_t));
     L->off_s2_rows = off;
@@ -136,9 +136,7 @@ int run_frames(const void *ref, const void *dis, int width, int height, int64_t 
     p.items_per_frame = L.items_per_frame;
     p.blocks_per_frame = L.blocks_per_frame;
     p.ctrl = reinterpret_cast<uint32_t *>(ws + L.off_ctrl);
-    p.done = p.ctrl + kCtrlWords;
-    p.block_done = p.done + nframes;
-    p.flags = p.block_done + (size_t)nframes * L.blocks_per_frame;
+    p.flags = p.ctrl + kCtrlWords;
     p.status = status_word ? status_word : p.ctrl + kCtrlStatus;
     p.items = reinterpret_cast<Agg *>(ws + L.off_items);
     p.blocks = reinterpret_cast<Agg *>(ws + L.off_blocks);

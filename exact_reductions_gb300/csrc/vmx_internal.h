@@ -20,8 +20,12 @@ constexpr int kWarps = kThreads / 32;
 #define VMX_UNROLL 4
 #endif
 constexpr int kMinBlocks = VMX_MIN_BLOCKS; // CTAs per SM the kernel is compiled for
-constexpr int kMaxRowsPerItem = 32;        // rows a warp takes per ticket, at most
-constexpr int kItemPixels = 4096;          // target pixels per warp item
+constexpr int kMaxRowsPerItem = 32;        // rows per item, at most
+constexpr int kMaxChunk = 4;               // items a warp takes per ticket, at most
+#ifndef VMX_ITEM_PIXELS
+#define VMX_ITEM_PIXELS 2048
+#endif
+constexpr int kItemPixels = VMX_ITEM_PIXELS; // target pixels per warp item
 constexpr int kUnroll = VMX_UNROLL;        // 16-byte vectors in flight per lane per plane
 constexpr uint32_t kSpinLimit = 1u << 22;  // bounded look-back wait (polls)
 
@@ -38,14 +42,16 @@ enum Ctrl : int {
 };
 
 // Per-item and per-block sums the walk reads (64 bytes): the exact
-// second-moment sums (ref, dis), the first-moment sums, the psnr sum, and the
-// odd-term counts (ref in the low half of odd, dis in the high half).
+// second-moment sums (ref, dis), the first-moment sums, the psnr sum, the
+// odd-term counts (ref in the low half of odd, dis in the high half) and, in
+// a block, how many of its items have added their sums.
 struct alignas(16) Agg {
     uint64_t s2[2];
     uint64_t s1[2];
     uint64_t psnr;
     uint64_t odd;
-    uint64_t pad[2];
+    uint64_t count;
+    uint64_t pad;
 };
 constexpr int kBlockItems = 32;  // items folded into one block aggregate
 
@@ -55,10 +61,10 @@ struct Layout {
     int rows_per_item, items_per_frame, blocks_per_frame;
     bool ordered;        // second moments may pass 2^53 units: odd counts per row
     bool full;           // ... and 2^55: look-back and row runs from binade 55 up
-    size_t off_ctrl;     // u32 [kCtrlWords] + done[F] + block_done[F * B] + flag[F * I]
-    size_t ctrl_bytes;   // bytes cleared per call
+    size_t off_ctrl;     // u32 [kCtrlWords] + flag[F * I]
+    size_t off_blocks;   // Agg [F * B], summed into by the items
+    size_t ctrl_bytes;   // bytes cleared per call: the control words and the blocks
     size_t off_items;    // Agg [F * I]
-    size_t off_blocks;   // Agg [F * B]
     size_t off_item_inc; // u64 [F * I][2] inclusive exact prefix per item (look-back)
     size_t off_s2_rows;  // u64 [F][2][H] (when the caller passes none)
     size_t off_odd_rows; // u32 [F][2][H] odd terms per row
@@ -76,7 +82,7 @@ struct Params {
     int width, height, frames;
     int k;            // bpc - 8
     int rows_per_item, items_per_frame, blocks_per_frame;
-    uint32_t *ctrl, *done, *block_done, *flags;
+    uint32_t *ctrl, *flags;
     uint32_t *status;  // set to 1 when a bounded wait gives up
     Agg *items, *blocks;
     uint64_t *item_inc;

@@ -67,6 +67,30 @@ __device__ __forceinline__ void st_release(uint32_t *ptr, uint32_t v)
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
+// Adds v at GPU scope with acquire-release order; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *ptr, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(ptr), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// Adds v at GPU scope with release order (no value returned).
+__device__ __forceinline__ void red_add_release(uint64_t *ptr, uint64_t v)
+{
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_acquire64(const uint64_t *ptr)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 // Sample type traits: a 16-byte vector holds 8 uint16 or 16 uint8 samples.
 template <typename TS>
 struct Samples;
@@ -275,21 +299,28 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
     Acc16 a = {};
     const int nvt = (width + 7) >> 3;
     for (int base = 0; base < nvt; base += 32 * kUnroll) {
+        // Vectors per lane this time (the same for the whole warp): kUnroll
+        // but at the row's end, where vectors past it are skipped.
+        const int nu = min(kUnroll, (nvt - base + 31) >> 5);
         uint4 R[kUnroll], D[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const int v = base + u * 32 + lane;
-            R[u] = load_vec<uint16_t, VEC>(rr, v, width);
-            D[u] = load_vec<uint16_t, VEC>(dr, v, width);
+            if (u < nu) {
+                const int v = base + u * 32 + lane;
+                R[u] = load_vec<uint16_t, VEC>(rr, v, width);
+                D[u] = load_vec<uint16_t, VEC>(dr, v, width);
+            }
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            acc16_word<M, P, ODD>(a, R[u].x, D[u].x);
-            acc16_word<M, P, ODD>(a, R[u].y, D[u].y);
-            acc16_word<M, P, ODD>(a, R[u].z, D[u].z);
-            acc16_word<M, P, ODD>(a, R[u].w, D[u].w);
+            if (u < nu) {
+                acc16_word<M, P, ODD>(a, R[u].x, D[u].x);
+                acc16_word<M, P, ODD>(a, R[u].y, D[u].y);
+                acc16_word<M, P, ODD>(a, R[u].z, D[u].z);
+                acc16_word<M, P, ODD>(a, R[u].w, D[u].w);
+            }
         }
-        acc16_flush<M, P, ODD>(a, 8 * kUnroll);
+        acc16_flush<M, P, ODD>(a, 8 * nu);
     }
     RowSums out = {0, 0, 0, 0, 0, 0, 0};
     if (M) {
@@ -681,7 +712,7 @@ __device__ __forceinline__ Agg load_agg(const Agg *a)
     g.s1[1] = ((uint64_t)w1.w << 32) | w1.z;
     g.psnr = ((uint64_t)w2.y << 32) | w2.x;
     g.odd = ((uint64_t)w2.w << 32) | w2.z;
-    g.pad[0] = g.pad[1] = 0;
+    g.count = g.pad = 0;
     return g;
 }
 
@@ -696,7 +727,7 @@ __device__ __forceinline__ void store_agg(Agg *a, const Agg &g)
                              (uint32_t)(g.odd >> 32)));
 }
 
-__device__ __forceinline__ Agg agg_zero() { return Agg{{0, 0}, {0, 0}, 0, 0, {0, 0}}; }
+__device__ __forceinline__ Agg agg_zero() { return Agg{{0, 0}, {0, 0}, 0, 0, 0, 0}; }
 
 __device__ __forceinline__ Agg agg_add(const Agg &a, const Agg &b)
 {
@@ -704,7 +735,8 @@ __device__ __forceinline__ Agg agg_add(const Agg &a, const Agg &b)
                {a.s1[0] + b.s1[0], a.s1[1] + b.s1[1]},
                a.psnr + b.psnr,
                a.odd + b.odd,
-               {0, 0}};
+               0,
+               0};
 }
 
 __device__ __forceinline__ Agg warp_sum_agg(Agg a)
@@ -721,6 +753,87 @@ __device__ __forceinline__ Agg warp_sum_agg(Agg a)
 __device__ __forceinline__ SC agg_sc(const Agg &a, int X)
 {
     return SC{a.s2[X], X ? (a.odd >> 32) : (a.odd & 0xffffffffull)};
+}
+
+// Items a block of frame blocks holds.
+__device__ __forceinline__ uint64_t block_items(const Params &p, int b)
+{
+    return (uint64_t)min(kBlockItems, p.items_per_frame - b * kBlockItems);
+}
+
+// Waits (bounded) until every block of frame f counts all its items, then
+// returns the frame's sums.
+__device__ Agg frame_totals(const Params &p, int f)
+{
+    const int lane = lane_id(), NB = p.blocks_per_frame;
+    const Agg *bl = p.blocks + (size_t)f * NB;
+    uint32_t spins = 0;
+    for (;;) {
+        bool ok = true;
+        for (int b = lane; b < NB; b += 32) ok = ok && ld_acquire64(&bl[b].count) >= block_items(p, b);
+        if (__all_sync(kFull, ok)) break;
+        if (++spins > p.spin_limit) {
+            if (lane == 0) atomicOr(p.status, 1u);
+            break;
+        }
+        __nanosleep(256);
+    }
+    Agg t = agg_zero();
+#pragma unroll 4
+    for (int i = lane; i < NB; i += 32) t = agg_add(t, load_agg(bl + i));
+    return warp_sum_agg(t);
+}
+
+// The first block of frame f whose inclusive exact prefix of plane X passes
+// 2^53, found as soon as the blocks up to it are complete (later blocks may
+// still be running); NB when the whole frame stays at or below 2^53. Waits
+// (bounded) while a block before the crossing is incomplete. *before gets
+// the prefix (sum, odd terms) before the block returned.
+__device__ int crossing_block(const Params &p, int f, int X, SC *before)
+{
+    const int lane = lane_id(), NB = p.blocks_per_frame;
+    const Agg *bl = p.blocks + (size_t)f * NB;
+    const int shift = X ? 32 : 0;
+    uint32_t spins = 0;
+    for (;;) {
+        SC run{0, 0};
+        bool ready = true;
+        for (int base = 0; base < NB; base += 32) {
+            count(p.ctrl, kCtrlPasses, 1);
+            const int b = base + lane;
+            bool done = true;
+            SC v{0, 0};
+            if (b < NB) {
+                done = ld_acquire64(&bl[b].count) >= block_items(p, b);
+                if (done) v = SC{__ldcg(&bl[b].s2[X]), (__ldcg(&bl[b].odd) >> shift) & 0xffffffffull};
+            }
+            const unsigned open = __ballot_sync(kFull, !done);
+            SC tot;
+            const SC ex = warp_excl_sc(v, &tot);
+            const unsigned hit = __ballot_sync(kFull, b < NB && done && run.s + ex.s + v.s > kTwo53);
+            const int first_open = open ? __ffs(open) - 1 : 32;
+            const int first_hit = hit ? __ffs(hit) - 1 : 32;
+            if (first_hit < first_open) {
+                *before = sc_add(run, shfl_sc(ex, first_hit));
+                return base + first_hit;
+            }
+            if (first_open < 32) {
+                ready = false;
+                break;
+            }
+            run = sc_add(run, tot);
+        }
+        if (ready) {
+            *before = run;
+            return NB;
+        }
+        if (++spins > p.spin_limit) {
+            if (lane == 0) atomicOr(p.status, 1u);
+            *before = run;
+            return NB;
+        }
+        __nanosleep(256);
+    }
 }
 
 // S after a run of terms with exact sum and odd count x, in the regime S is
@@ -756,20 +869,22 @@ __device__ uint64_t resolve_row_fast(const unsigned char *row, int width, uint64
         uint4 V[8];
 #pragma unroll
         for (int v = 0; v < 8; ++v) V[v] = load_vec<uint16_t, true>(row, (j0 >> 3) + v, width);
-        uint64_t ls = 0, lc = 0;
+        uint64_t ls = 0;
+        uint32_t lc32 = 0;  // at most 64: a 32-bit count keeps the chains short
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
             const uint32_t w4[4] = {V[v].x, V[v].y, V[v].z, V[v].w};
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int j = j0 + v * 8 + k;
-                const uint32_t t = term_of_sample((w4[k >> 1] >> (16 * (k & 1))) & 0xffffu);
-                if (j >= pos && j < width) {
-                    ls += t;
-                    lc += t & 1u;
-                }
+                const uint32_t t = (j >= pos && j < width)
+                                       ? term_of_sample((w4[k >> 1] >> (16 * (k & 1))) & 0xffffu)
+                                       : 0u;
+                ls += t;
+                lc32 += t & 1u;
             }
         }
+        const uint64_t lc = lc32;
         SC tot;
         const SC ex = warp_excl_sc(SC{ls, lc}, &tot);
         const bool exact = S < kTwo53;
@@ -831,28 +946,29 @@ __device__ uint64_t resolve_row_fast(const unsigned char *row, int width, uint64
     return S;
 }
 
-// The common case of a plane past 2^53 units: the first row whose exact
-// prefix passes 2^53 is found by narrowing blocks, items and rows (one pass
-// each); that row is walked term by term; all later rows are added by one
-// closed form if the sum then stays in its binade (always so below 2^55).
-// Anything else continues on the general path.
+// The second-moment sum of plane X. The first block whose exact prefix
+// passes 2^53 is found as soon as the blocks before it are complete, then
+// its item and row (one pass each); that row is walked term by term while
+// the frame's later rows may still be running. Once the frame is complete,
+// all later rows are added by one closed form if the sum then stays in its
+// binade (always so below 2^55); anything else continues on the general
+// path. *t gets the frame's sums.
 template <typename TS, bool VEC, bool FULL>
-__device__ uint64_t walk_plane_fast(const Params &p, int f, int X, uint64_t tot, uint64_t tot_odd)
+__device__ uint64_t walk_plane_fast(const Params &p, int f, int X, Agg *t)
 {
-    const int I = p.items_per_frame, NB = p.blocks_per_frame, H = p.height;
-    const Agg *blocks = p.blocks + (size_t)f * NB;
+    const int I = p.items_per_frame, H = p.height;
     const Agg *items = p.items + (size_t)f * I;
     const size_t off = ((size_t)f * 2 + X) * H;
     const uint64_t *R = p.s2_rows + off;
     const uint32_t *O = p.odd_rows + off;
     const uint64_t hi_mask = X ? 32 : 0;
     SC b0;
-    const int blk = warp_first(
-        [blocks, X, hi_mask](int i) {
-            return SC{__ldcg(&blocks[i].s2[X]), (__ldcg(&blocks[i].odd) >> hi_mask) & 0xffffffffull};
-        },
-        0, NB, [](SC x) { return x.s > kTwo53; }, &b0, p.ctrl);
-    if (blk >= NB) return tot;  // cannot happen: tot > 2^53
+    const int blk = crossing_block(p, f, X, &b0);
+    if (blk >= p.blocks_per_frame) {
+        *t = frame_totals(p, f);
+        count(p.ctrl, kCtrlRowsExact, (uint32_t)H);
+        return t->s2[X];
+    }
     SC b1;
     const int it = warp_first(
         [items, X, hi_mask](int i) {
@@ -875,6 +991,8 @@ __device__ uint64_t walk_plane_fast(const Params &p, int f, int X, uint64_t tot,
     else S = resolve_row<TS>(rp, p.width, S, p.ctrl);
     count(p.ctrl, kCtrlRowsTerms, 1);
     const uint64_t rs = __ldcg(R + row), rc = __ldcg(O + row);
+    *t = frame_totals(p, f);
+    const uint64_t tot = t->s2[X], tot_odd = X ? (t->odd >> 32) : (t->odd & 0xffffffffull);
     const uint64_t rest_s = tot - pre.s - rs, rest_c = tot_odd - pre.c - rc;
     if (S >= kTwo53 && binade_of(S) <= 54) {
         const int b = binade_of(S);
@@ -892,26 +1010,26 @@ __device__ uint64_t walk_plane_fast(const Params &p, int f, int X, uint64_t tot,
 template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC>
 __device__ __noinline__ void walk_part(const Params &p, int f, int part)
 {
-    const int NB = p.blocks_per_frame;
-    const Agg *bl = p.blocks + (size_t)f * NB;
-    Agg t = agg_zero();
-#pragma unroll 4
-    for (int i = lane_id(); i < NB; i += 32) t = agg_add(t, load_agg(bl + i));
-    t = warp_sum_agg(t);
     const double N = (double)p.width * (double)p.height;
     const bool lead = lane_id() == 0;
     if (M && part < 2) {
         const int X = part;
-        uint64_t s2 = t.s2[X];
-        const uint64_t odd = X ? (t.odd >> 32) : (t.odd & 0xffffffffull);
-        if (ODD && s2 > kTwo53) s2 = walk_plane_fast<TS, VEC, FULL>(p, f, X, t.s2[X], odd);
-        else count(p.ctrl, kCtrlRowsExact, (uint32_t)p.height);
+        Agg t;
+        uint64_t s2;
+        if (ODD) {
+            s2 = walk_plane_fast<TS, VEC, FULL>(p, f, X, &t);
+        } else {  // such frames stay at or below 2^53 units
+            t = frame_totals(p, f);
+            s2 = t.s2[X];
+            count(p.ctrl, kCtrlRowsExact, (uint32_t)p.height);
+        }
         if (lead) {
             p.moments[(size_t)f * 4 + X] = scaled_mean(t.s1[X], p.k, N);
             p.moments[(size_t)f * 4 + 2 + X] = scaled_mean(s2, 2 * p.k, N);
             if (p.s2_sums) p.s2_sums[(size_t)f * 2 + X] = s2;
         }
     } else if (P) {
+        const Agg t = frame_totals(p, f);
         const uint64_t d = t.psnr <= kTwo53 ? t.psnr
                                             : walk_rows(p.psnr_rows + (size_t)f * p.height, p.height, p.ctrl);
         if (lead) {
@@ -972,20 +1090,38 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
     const int I = p.items_per_frame, NB = p.blocks_per_frame;
     const int nitems = p.frames * I;
     const int H = p.height;
+    // Items are handed out in chunks of consecutive items, one atomic per
+    // chunk, the chunk size shrinking from kMaxChunk to 1 as the items run
+    // out. Without look-back each warp's first item is its own index and the
+    // counter hands out the rest. Waits stay deadlock-free: a warp works
+    // through its chunk in order, so the smallest unfinished item is always
+    // some warp's current item.
+    const uint32_t nwarps = gridDim.x * (uint32_t)kWarps;
+    const uint32_t gwarp = blockIdx.x * (uint32_t)kWarps + (threadIdx.x >> 5);
+    const uint32_t first = FULL ? 0u : nwarps;  // tickets below are assigned
+    uint32_t cur = FULL ? 0u : gwarp, end = FULL ? 0u : gwarp + 1, seen = first;
     for (;;) {
-        int tk = 0;
-        if (lane == 0) tk = (int)atomicAdd(p.ctrl + kCtrlTicket, 1u);
-        tk = __shfl_sync(kFull, tk, 0);
+        if (cur >= end) {
+            const uint32_t left = (uint32_t)nitems > seen ? (uint32_t)nitems - seen : 0u;
+            const uint32_t k = max(1u, min((uint32_t)kMaxChunk, left / (4u * nwarps)));
+            uint32_t c = 0;
+            if (lane == 0) c = atomicAdd(p.ctrl + kCtrlTicket, k);
+            c = __shfl_sync(kFull, c, 0) + first;
+            seen = c + k;
+            cur = c;
+            end = c + k;
+        }
+        const int tk = (int)cur++;
         if (tk >= nitems) break;
         const int f = tk / I, j = tk - f * I;
         const int r0 = j * p.rows_per_item, r1 = min(H, r0 + p.rows_per_item);
         const unsigned char *fr = p.ref + (int64_t)f * p.pitch;
         const unsigned char *fd = p.dis + (int64_t)f * p.pitch;
 
-        // A. exact row sums. Lane 0 records each row; the item's sums are
-        // then read back from those records, one lane per row, so that no
-        // item totals stay live across the rows.
+        // A. exact row sums. Lane 0 records each row; lane i keeps the sums
+        // of the item's row i, so that no item totals stay live across rows.
         uint32_t s1r = 0, s1d = 0;  // this lane's first-moment sums
+        uint64_t my_r = 0, my_d = 0, my_p = 0, my_o = 0;
         for (int r = r0; r < r1; ++r) {
             const unsigned char *rr = fr + (int64_t)r * p.stride;
             const unsigned char *dr = fd + (int64_t)r * p.stride;
@@ -1004,21 +1140,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
             }
             s1r += (uint32_t)rs.s1r;
             s1d += (uint32_t)rs.s1d;
-        }
-        __syncwarp();
-        Agg g = agg_zero();
-        uint64_t my_r = 0, my_d = 0, my_p = 0, my_o = 0;  // this lane's row (lane < rows)
-        if (lane < r1 - r0) {
-            const int r = r0 + lane;
-            if (M) {
-                my_r = __ldcg(p.s2_rows + ((size_t)f * 2) * H + r);
-                my_d = __ldcg(p.s2_rows + ((size_t)f * 2 + 1) * H + r);
+            if (lane == r - r0) {
+                my_r = rs.t2r;
+                my_d = rs.t2d;
+                my_p = rs.tp;
+                my_o = (uint64_t)rs.oddr | ((uint64_t)rs.oddd << 32);
             }
-            if (ODD)
-                my_o = (uint64_t)__ldcg(p.odd_rows + ((size_t)f * 2) * H + r) |
-                       ((uint64_t)__ldcg(p.odd_rows + ((size_t)f * 2 + 1) * H + r) << 32);
-            if (P) my_p = __ldcg(p.psnr_rows + (size_t)f * H + r);
         }
+        Agg g = agg_zero();
         if (M) {
             g.s2[0] = warp_sum(my_r);
             g.s2[1] = warp_sum(my_d);
@@ -1062,32 +1191,26 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
             }
         }
 
-        // C. completion: the warp that finishes a block of items folds it;
-        // the warp that folds a frame's last block walks the frame.
-        const int blk = j / kBlockItems;
-        int last = 0;
+        // C. completion: the item's sums go into its block's sums, then the
+        // block's count of finished items (release: after all of the above).
         if (lane == 0) {
-            __threadfence();
-            const uint32_t n = (uint32_t)min(kBlockItems, I - blk * kBlockItems);
-            last = atomicAdd(p.block_done + (size_t)f * NB + blk, 1u) + 1 == n;
-        }
-        if (__shfl_sync(kFull, last, 0)) {
-            __threadfence();
-            const int i = blk * kBlockItems + lane;
-            Agg a = i < I ? load_agg(p.items + (size_t)f * I + i) : agg_zero();
-            a = warp_sum_agg(a);
-            if (lane == 0) {
-                store_agg(p.blocks + (size_t)f * NB + blk, a);
-                __threadfence();
-                atomicAdd(p.done + f, 1u);
+            Agg *b = p.blocks + (size_t)f * NB + j / kBlockItems;
+            if (M) {
+                atomicAdd(reinterpret_cast<unsigned long long *>(&b->s2[0]), g.s2[0]);
+                atomicAdd(reinterpret_cast<unsigned long long *>(&b->s2[1]), g.s2[1]);
+                atomicAdd(reinterpret_cast<unsigned long long *>(&b->s1[0]), g.s1[0]);
+                atomicAdd(reinterpret_cast<unsigned long long *>(&b->s1[1]), g.s1[1]);
             }
+            if (ODD) atomicAdd(reinterpret_cast<unsigned long long *>(&b->odd), g.odd);
+            if (P) atomicAdd(reinterpret_cast<unsigned long long *>(&b->psnr), g.psnr);
+            red_add_release(&b->count, 1ull);
         }
     }
 
     // D. Walks. A warp out of items takes a part of a frame to walk (the ref
-    // moments, the dis moments, the psnr noise); it waits (bounded) until
-    // the frame's blocks are all folded: those are held by warps that are
-    // running and wait on nothing here.
+    // moments, the dis moments, the psnr noise). Its waits on the frame's
+    // blocks are bounded; the items they wait for are held by warps that are
+    // running, or by blocks not yet resident that start as others retire.
     constexpr int kParts = (M ? 2 : 0) + (P ? 1 : 0);
     for (;;) {
         int wt = 0;
@@ -1095,19 +1218,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         wt = __shfl_sync(kFull, wt, 0);
         if (wt >= p.frames * kParts) break;
         const int wf = wt / kParts, part = wt - wf * kParts;
-        if (lane == 0) {
-            uint32_t spins = 0;
-            while (ld_acquire(p.done + wf) < (uint32_t)NB) {
-                if (++spins > p.spin_limit) {
-                    atomicOr(p.status, 1u);
-                    break;
-                }
-                __nanosleep(128);
-            }
-            __threadfence();
-        }
-        __syncwarp();
-        __threadfence();
         walk_part<TS, M, P, ODD, FULL, VEC>(p, wf, M ? part : 2);
     }
 }
