@@ -129,15 +129,35 @@ class Clocks:
                 "reasons": sorted(reasons)}
 
 
+def frame_indices(rank: int, frames: int) -> range:
+    """Rank r takes frames r*F .. r*F+F-1 of the workload's seeded stream."""
+    return range(rank * frames, (rank + 1) * frames)
+
+
+def max_over_ranks(x: float, pg) -> float:
+    """The largest x over the ranks of pg (x itself when pg is None)."""
+    if pg is None:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=pg)
+    return float(t[0])
+
+
+def whole_job_rate(world: int, frames_per_rank: int, steps: int, seconds: float) -> float:
+    """Frames of all ranks over the slowest rank's time."""
+    return world * frames_per_rank * steps / seconds
+
+
 def make_batch(rank: int):
     from exact_reductions_gb300 import synth
     wl = synth.WORKLOADS[WORKLOAD]
     F = wl.frames
     ref = np.empty((F, wl.height, wl.width), dtype=np.uint16)
     dis = np.empty_like(ref)
-    for f in range(F):
-        # Rank r takes frames r*F .. r*F+F-1 of the workload's seeded stream.
-        ref[f], dis[f] = wl.frame(rank * F + f)
+    for i, f in enumerate(frame_indices(rank, F)):
+        ref[i], dis[i] = wl.frame(f)
     return wl, ref, dis
 
 
@@ -260,30 +280,25 @@ def run_ours(args, rank, local_rank, world, pg):
     launches = api.kernel_launches() - launches0
     assert api.workspace_status(ws) == 0, "bounded device wait gave up"
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
-    device_ms = starts[0].elapsed_time(ends[-1])
-    t = torch.tensor([device_ms], dtype=torch.float64)
-    if pg is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX, group=pg)
-    device_ms = float(t[0])
-    value = world * F * args.steps / (device_ms / 1e3)
+    device_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), pg)
+    value = whole_job_rate(world, F, args.steps, device_ms / 1e3)
 
-    # End to end through the host-memory entry point: pinned host frames in,
-    # results out, copies inside the timed call.
-    pin_r = torch.from_numpy(ref_h).pin_memory().numpy()
-    pin_d = torch.from_numpy(dis_h).pin_memory().numpy()
-    e2e_steps = max(1, min(args.steps, 5))
-    hws = None
-    out = api.frames_host(pin_r, pin_d, wl.bpc, features=3, chunk_frames=2)
+    # End to end through the host-memory entry point: pinned host frames in
+    # (read in place by the kernel over the host link), results out, all
+    # inside the timed call; one launch for the 16 frames.
+    pin_r = torch.from_numpy(ref_h).pin_memory()
+    pin_d = torch.from_numpy(dis_h).pin_memory()
+    e2e_steps = max(1, min(args.steps, 10))
+    hws = api.workspace(api.host_workspace_bytes(wl.width, wl.height, wl.width * 2, wl.bpc, F, 3),
+                        dev)
+    out = api.frames_host(pin_r.numpy(), pin_d.numpy(), wl.bpc, features=3, chunk_frames=F, ws=hws)
     torch.cuda.synchronize()
     t1 = time.perf_counter()
     for _ in range(e2e_steps):
-        out = api.frames_host(pin_r, pin_d, wl.bpc, features=3, chunk_frames=2, ws=hws)
-    e2e_s = (time.perf_counter() - t1) / e2e_steps
+        out = api.frames_host(pin_r.numpy(), pin_d.numpy(), wl.bpc, features=3, chunk_frames=F,
+                              ws=hws)
+    e2e_s = max_over_ranks((time.perf_counter() - t1) / e2e_steps, pg)
     h2d, d2h = api.host_traffic(wl.width, wl.height, wl.width * 2, wl.bpc, F, 3)
-    e = torch.tensor([e2e_s], dtype=torch.float64)
-    if pg is not None:
-        dist.all_reduce(e, op=dist.ReduceOp.MAX, group=pg)
-    e2e_s = float(e[0])
     if rank != 0:
         return
 
@@ -304,7 +319,7 @@ def run_ours(args, rank, local_rank, world, pg):
                      "kernel": "frames_kernel (one launch per step)",
                      "algorithmic_bytes_per_launch": bytes_per_launch,
                      "avg_launch_ms": avg_ms},
-        "e2e": {"value": world * F / e2e_s, "unit": "frames/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_rate(world, F, 1, e2e_s), "unit": "frames/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),
@@ -314,6 +329,65 @@ def run_ours(args, rank, local_rank, world, pg):
     print(json.dumps(line), flush=True)
 
 
+def run_configs(args):
+    """One JSON line per workload (C1..C5c): GPU frames/s and GB/s with
+    inputs resident, the oracle on the host cores (one core, and all cores
+    one frame per thread), and whether the GPU outputs equal the oracle's
+    on the frames the oracle computed."""
+    import torch
+
+    import __graft_entry__
+    import oracle
+    from exact_reductions_gb300 import api, synth
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    peak, peak_kind = peak_hbm()
+    threads = os.cpu_count() or 1
+    for key in ("C1", "C2", "C3", "C4", "C5a", "C5b", "C5c"):
+        wl = synth.WORKLOADS[key]
+        ref, dis = wl.batch()
+        F = ref.shape[0]
+        R = torch.from_numpy(ref).to(dev)
+        D = torch.from_numpy(dis).to(dev)
+        out = api.frames(R, D, wl.bpc, features=3)
+        ws = out["_workspace"]
+        for _ in range(3):
+            out = api.frames(R, D, wl.bpc, features=3, ws=ws)
+        torch.cuda.synchronize()
+        reps = args.steps if args.steps < 50 else 20
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):  # back to back, as a stream of batches runs
+            out = api.frames(R, D, wl.bpc, features=3, ws=ws)
+        e.record()
+        torch.cuda.synchronize()
+        t = s.elapsed_time(e) / 1e3 / reps
+        status = api.workspace_status(ws)
+        got_m = out["moments"].cpu().numpy()
+        got_mse = out["mse"].cpu().numpy()
+        # The oracle: one frame on one core, then min(cores, F) frames at once.
+        n1 = 1
+        t0 = time.perf_counter()
+        oracle.batch(ref[:n1], dis[:n1], wl.bpc, threads=1)
+        one_core = (time.perf_counter() - t0) / n1
+        n = min(threads, F)
+        t0 = time.perf_counter()
+        want = oracle.batch(ref[:n], dis[:n], wl.bpc, threads=threads)
+        all_cores = n / (time.perf_counter() - t0)
+        exact = bool(np.array_equal(want["moments"].view(np.uint64), got_m[:n].view(np.uint64)) and
+                     np.array_equal(want["mse"].view(np.uint64), got_mse[:n].view(np.uint64)))
+        gbs = F * wl.frame_pair_bytes / t / 1e9
+        print(json.dumps({
+            "workload": f"{key}: {F} x {wl.width}x{wl.height} {wl.bpc}-bit", "frames_per_s": F / t,
+            "ms_per_call": t * 1e3, "gb_per_s": gbs, "frac_of_peak": gbs / peak,
+            "peak": f"{peak} GB/s ({peak_kind})", "oracle_ms_per_frame_1core": one_core * 1e3,
+            "oracle_frames_per_s_all_cores": all_cores, "oracle_cores": min(threads, n),
+            "bit_exact_frames_checked": n, "bit_exact": exact and status == 0}), flush=True)
+        del R, D, out, ws
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -321,7 +395,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--configs", action="store_true",
+                    help="one line per workload C1..C5c (GPU, oracle, bit-exactness) instead")
     args = ap.parse_args()
+    if args.configs:
+        run_configs(args)
+        return
     rank, local_rank, world = dist_env()
     pg = None
     if world > 1:

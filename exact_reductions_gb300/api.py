@@ -57,6 +57,12 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else t.data_ptr()
 
 
+def host_workspace_bytes(width: int, height: int, stride_bytes: int, bpc: int, chunk_frames: int,
+                         features: int) -> int:
+    return int(_lib.load().vmx_host_workspace_bytes(width, height, stride_bytes, bpc, chunk_frames,
+                                                    features))
+
+
 def workspace_bytes(width: int, height: int, bpc: int, frames: int, features: int) -> int:
     return int(_lib.load().vmx_workspace_bytes(width, height, bpc, frames, features))
 

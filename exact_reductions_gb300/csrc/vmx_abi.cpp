@@ -327,6 +327,26 @@ bool host_plan(int width, int height, int64_t stride, int bpc, int chunk, int fe
     return true;
 }
 
+// The device's address for `bytes` of host memory at ptr when the device can
+// read all of it in place (page-locked, mapped memory), else false.
+bool device_view(const void *ptr, size_t bytes, const unsigned char **dev)
+{
+    cudaPointerAttributes a, b;
+    const unsigned char *p = static_cast<const unsigned char *>(ptr);
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess ||
+        cudaPointerGetAttributes(&b, p + (bytes - 1)) != cudaSuccess) {
+        cudaGetLastError();  // not an error for the call: use staged copies
+        return false;
+    }
+    if (a.type != cudaMemoryTypeHost || b.type != cudaMemoryTypeHost || !a.devicePointer ||
+        !b.devicePointer)
+        return false;
+    const unsigned char *d = static_cast<const unsigned char *>(a.devicePointer);
+    if (static_cast<const unsigned char *>(b.devicePointer) != d + (bytes - 1)) return false;
+    *dev = d;
+    return true;
+}
+
 }  // namespace
 
 size_t vmx_host_workspace_bytes(int width, int height, int64_t stride_bytes, int bpc,
@@ -381,31 +401,43 @@ int vmx_frames_host(const void *ref, const void *dis, int width, int height,
         if (err != cudaSuccess) return cuda_fail(err);
         ws = static_cast<unsigned char *>(p);
     }
-    err = cudaStreamCreateWithFlags(&copy, cudaStreamNonBlocking);
-    for (int s = 0; s < 2 && err == cudaSuccess; ++s) {
-        err = cudaEventCreateWithFlags(&copied[s], cudaEventDisableTiming);
-        if (err == cudaSuccess) err = cudaEventCreateWithFlags(&computed[s], cudaEventDisableTiming);
+    const size_t H = (size_t)height;
+    const size_t frame_bytes = H * (size_t)stride_bytes;
+    // Page-locked inputs are read in place by the kernel (over the host link,
+    // no staging copy); others are copied chunk by chunk into the workspace.
+    const unsigned char *zr = nullptr, *zd = nullptr;
+    const bool in_place = device_view(ref, (size_t)nframes * frame_bytes, &zr) &&
+                          device_view(dis, (size_t)nframes * frame_bytes, &zd);
+    if (!in_place) {
+        err = cudaStreamCreateWithFlags(&copy, cudaStreamNonBlocking);
+        for (int s = 0; s < 2 && err == cudaSuccess; ++s) {
+            err = cudaEventCreateWithFlags(&copied[s], cudaEventDisableTiming);
+            if (err == cudaSuccess)
+                err = cudaEventCreateWithFlags(&computed[s], cudaEventDisableTiming);
+        }
     }
     uint32_t *dstatus = reinterpret_cast<uint32_t *>(ws + hp.off_status);
     if (err == cudaSuccess) err = cudaMemsetAsync(dstatus, 0, sizeof(uint32_t), cs);
-    const size_t H = (size_t)height;
-    const size_t frame_bytes = H * (size_t)stride_bytes;
     for (int c0 = 0, it = 0; c0 < nframes && err == cudaSuccess && status == VMX_OK;
          c0 += chunk, ++it) {
         const int n = std::min(chunk, nframes - c0);
-        const int slot = it & 1;
-        unsigned char *in_r = ws + hp.off_in[slot][0], *in_d = ws + hp.off_in[slot][1];
+        const int slot = in_place ? 0 : it & 1;
+        const unsigned char *in_r = in_place ? zr + c0 * frame_bytes : ws + hp.off_in[slot][0];
+        const unsigned char *in_d = in_place ? zd + c0 * frame_bytes : ws + hp.off_in[slot][1];
         unsigned char *out = ws + hp.off_out[slot];
-        // Inputs of this chunk: wait until the slot's previous chunk computed.
-        if (it >= 2) err = cudaStreamWaitEvent(copy, computed[slot], 0);
-        if (err == cudaSuccess)
-            err = cudaMemcpyAsync(in_r, static_cast<const unsigned char *>(ref) + c0 * frame_bytes,
-                                  n * frame_bytes, cudaMemcpyHostToDevice, copy);
-        if (err == cudaSuccess)
-            err = cudaMemcpyAsync(in_d, static_cast<const unsigned char *>(dis) + c0 * frame_bytes,
-                                  n * frame_bytes, cudaMemcpyHostToDevice, copy);
-        if (err == cudaSuccess) err = cudaEventRecord(copied[slot], copy);
-        if (err == cudaSuccess) err = cudaStreamWaitEvent(cs, copied[slot], 0);
+        if (!in_place) {
+            // Inputs of this chunk: wait until the slot's previous chunk computed.
+            unsigned char *sr = ws + hp.off_in[slot][0], *sd = ws + hp.off_in[slot][1];
+            if (it >= 2) err = cudaStreamWaitEvent(copy, computed[slot], 0);
+            if (err == cudaSuccess)
+                err = cudaMemcpyAsync(sr, static_cast<const unsigned char *>(ref) + c0 * frame_bytes,
+                                      n * frame_bytes, cudaMemcpyHostToDevice, copy);
+            if (err == cudaSuccess)
+                err = cudaMemcpyAsync(sd, static_cast<const unsigned char *>(dis) + c0 * frame_bytes,
+                                      n * frame_bytes, cudaMemcpyHostToDevice, copy);
+            if (err == cudaSuccess) err = cudaEventRecord(copied[slot], copy);
+            if (err == cudaSuccess) err = cudaStreamWaitEvent(cs, copied[slot], 0);
+        }
         if (err != cudaSuccess) break;
         Outputs o;
         o.moments = m ? reinterpret_cast<double *>(out + hp.o_moments) : nullptr;
@@ -430,7 +462,7 @@ int vmx_frames_host(const void *ref, const void *dis, int width, int height,
             if (err == cudaSuccess)
                 err = cudaMemcpyAsync(mse + c0, o.mse, n * sizeof(double), cudaMemcpyDeviceToHost, cs);
         }
-        if (err == cudaSuccess) err = cudaEventRecord(computed[slot], cs);
+        if (err == cudaSuccess && !in_place) err = cudaEventRecord(computed[slot], cs);
     }
     // A bounded wait that gave up in any chunk fails the call.
     uint32_t st = 0;

@@ -1093,7 +1093,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
     // Items are handed out in chunks of consecutive items, one atomic per
     // chunk, the chunk size shrinking from kMaxChunk to 1 as the items run
     // out. Without look-back each warp's first item is its own index and the
-    // counter hands out the rest. Waits stay deadlock-free: a warp works
+    // counter hands out the rest. With look-back a chunk is one item: an
+    // item's look-back waits for the item before it, and in a longer chunk
+    // that item would wait for its owner's earlier items, so the chunks
+    // would run one after another. Waits stay deadlock-free: a warp works
     // through its chunk in order, so the smallest unfinished item is always
     // some warp's current item.
     const uint32_t nwarps = gridDim.x * (uint32_t)kWarps;
@@ -1103,7 +1106,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
     for (;;) {
         if (cur >= end) {
             const uint32_t left = (uint32_t)nitems > seen ? (uint32_t)nitems - seen : 0u;
-            const uint32_t k = max(1u, min((uint32_t)kMaxChunk, left / (4u * nwarps)));
+            const uint32_t k = FULL ? 1u : max(1u, min((uint32_t)kMaxChunk, left / (4u * nwarps)));
             uint32_t c = 0;
             if (lane == 0) c = atomicAdd(p.ctrl + kCtrlTicket, k);
             c = __shfl_sync(kFull, c, 0) + first;

@@ -137,12 +137,13 @@ int vmx_workspace_stats(const void *workspace, void *stream, uint64_t *out4);
 int vmx_psnr_db(const double *mse, int n, int bpc, double psnr_max, double *psnr);
 
 /*
- * Host-memory entry point: frames in host memory (page-locked memory lets
- * the copies overlap the kernels), results in host memory, same layout and
- * outputs as the device calls. Chunks of `chunk_frames` frames are copied to
- * the device on a stream the call creates while the previous chunk computes
- * on `stream`; each chunk's results are copied back on `stream`. Returns
- * after everything has finished. features: VMX_FEATURE_* bits; outputs of a
+ * Host-memory entry point: frames in host memory, results in host memory,
+ * same layout and outputs as the device calls, `chunk_frames` frames per
+ * launch on `stream`. Page-locked (mapped) inputs are read in place by the
+ * kernel over the host link, with no staging copy; other host memory is
+ * copied chunk by chunk into the workspace on a stream the call creates
+ * while the previous chunk computes. Each chunk's results are copied back
+ * on `stream`. Returns after everything has finished. features: VMX_FEATURE_* bits; outputs of a
  * feature not asked for may be NULL, as may s2_rows and psnr (psnr needs
  * VMX_FEATURE_PSNR; it is vmx_psnr_db() of mse with psnr_max).
  *   workspace  device memory of vmx_host_workspace_bytes(...) bytes, 256-byte

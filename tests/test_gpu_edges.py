@@ -104,6 +104,28 @@ def test_host_entry_matches_device_entry():
     assert same_doubles(host["psnr"], [oracle.psnr_db(m, 16, 0.0) for m in want_mse])
 
 
+@pytest.mark.parametrize("chunk", [2, 5])
+def test_host_entry_reads_pinned_frames_in_place(chunk):
+    """Page-locked host frames are read in place by the kernel (no staging
+    copy); the outputs equal the device call's and the pageable call's."""
+    wl = synth.WORKLOADS["C5a"]
+    ref, dis = wl.batch(5)
+    pin_r = torch.from_numpy(ref).pin_memory()
+    pin_d = torch.from_numpy(dis).pin_memory()
+    assert pin_r.is_pinned() and pin_d.is_pinned()
+    pinned = api.frames_host(pin_r.numpy(), pin_d.numpy(), 16, features=3, chunk_frames=chunk,
+                             s2_rows=True)
+    pageable = api.frames_host(ref, dis, 16, features=3, chunk_frames=chunk, s2_rows=True)
+    dev = api.frames(to_device(ref), to_device(dis), 16, s2_rows=True)
+    torch.cuda.synchronize()
+    for k in ("moments", "mse", "psnr"):
+        assert same_doubles(pinned[k], pageable[k]), k
+    for k in ("psnr_rows", "s2_rows"):
+        assert np.array_equal(pinned[k], pageable[k]), k
+    assert same_doubles(pinned["moments"], dev["moments"].cpu().numpy())
+    assert np.array_equal(pinned["s2_rows"], u64(dev["s2_rows"]))
+
+
 def test_launch_counter_counts_calls():
     wl = synth.WORKLOADS["C1"]
     ref, dis = wl.batch()
