@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <climits>
 #include <cmath>
 #include <cstdio>
@@ -19,6 +20,18 @@ namespace vmx {
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
+
+// Launch numbers: distinct per launch and, starting from the clock and an
+// address of this library, unlike anything an earlier process left in the
+// same memory. Items carry the number of the launch that wrote them.
+uint64_t next_launch_number()
+{
+    static std::atomic<uint64_t> seq{
+        ((uint64_t)std::chrono::steady_clock::now().time_since_epoch().count() << 20) ^
+        (uint64_t)(uintptr_t)&g_launches};
+    const uint64_t v = seq.fetch_add(1, std::memory_order_relaxed);
+    return v ? v : seq.fetch_add(1, std::memory_order_relaxed);
+}
 thread_local char g_last_cuda[160] = "";
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -150,6 +163,7 @@ int run_frames(const void *ref, const void *dis, int width, int height, int64_t 
     p.s2_sums = o.s2_sums;
     p.noise_sums = o.noise_sums;
     p.spin_limit = kSpinLimit;
+    p.launch = next_launch_number();
     const bool vec = (uintptr_t)ref % 16 == 0 && (uintptr_t)dis % 16 == 0 && stride % 16 == 0;
     err = cudaMemsetAsync(ws + L.off_ctrl, 0, L.ctrl_bytes, stream);
     if (err == cudaSuccess) {

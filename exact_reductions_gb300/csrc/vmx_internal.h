@@ -44,7 +44,8 @@ enum Ctrl : int {
 // Per-item and per-block sums the walk reads (64 bytes): the exact
 // second-moment sums (ref, dis), the first-moment sums, the psnr sum, the
 // odd-term counts (ref in the low half of odd, dis in the high half) and, in
-// a block, how many of its items have added their sums.
+// a block, how many of its items have added their sums; in an item, the
+// number of the launch that wrote it.
 struct alignas(16) Agg {
     uint64_t s2[2];
     uint64_t s1[2];
@@ -92,6 +93,7 @@ struct Params {
     double *moments, *mse;
     uint64_t *s2_sums, *noise_sums;
     uint32_t spin_limit;
+    uint64_t launch;  // this launch's number (never 0): stamps finished items
 };
 
 // Enqueue the frame kernel. `features` VMX_FEATURE_* bits; `vec` true when

@@ -84,6 +84,11 @@ __device__ __forceinline__ void red_add_release(uint64_t *ptr, uint64_t v)
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_release64(uint64_t *ptr, uint64_t v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ uint64_t ld_acquire64(const uint64_t *ptr)
 {
     uint64_t v;
@@ -133,6 +138,13 @@ __device__ __forceinline__ uint4 load_vec(const unsigned char *row, int v, int w
 // ------------------------------------------------------- warp primitives ---
 
 __device__ __forceinline__ int lane_id() { return (int)(threadIdx.x & 31); }
+
+__device__ __forceinline__ uint32_t warp_sum32(uint32_t v)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+    return v;
+}
 
 __device__ __forceinline__ uint64_t warp_sum(uint64_t v)
 {
@@ -262,8 +274,9 @@ __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
 }
 
 // Moves one iteration's sums to the row sums. `slots` samples per plane went
-// into them: at most 32 per lane keeps every 32-bit sum below 2^30 and every
-// odd-term byte below 2^8.
+// into them: at most 64 per lane keeps every 32-bit sum below 2^30 (64 times
+// 65535 times 255), every error sum below 2^13 and every odd-term byte below
+// 2^8.
 template <bool M, bool P, bool ODD>
 __device__ __forceinline__ void acc16_flush(Acc16 &a, uint32_t slots)
 {
@@ -294,14 +307,19 @@ __device__ __forceinline__ void acc16_flush(Acc16 &a, uint32_t slots)
 template <bool M, bool P, bool ODD, bool VEC>
 __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, int width)
 {
-    static_assert(kUnroll * 8 <= 32, "flush before 32 samples per lane");
+    static_assert(kUnroll * 8 <= 64, "an iteration holds at most 64 samples per lane");
     const int lane = lane_id();
     Acc16 a = {};
     const int nvt = (width + 7) >> 3;
+    uint32_t pend = 0;  // samples per lane per plane since the last flush
     for (int base = 0; base < nvt; base += 32 * kUnroll) {
         // Vectors per lane this time (the same for the whole warp): kUnroll
         // but at the row's end, where vectors past it are skipped.
         const int nu = min(kUnroll, (nvt - base + 31) >> 5);
+        if (pend + 8 * nu > 64) {
+            acc16_flush<M, P, ODD>(a, pend);
+            pend = 0;
+        }
         uint4 R[kUnroll], D[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -320,8 +338,9 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
                 acc16_word<M, P, ODD>(a, R[u].w, D[u].w);
             }
         }
-        acc16_flush<M, P, ODD>(a, 8 * nu);
+        pend += 8 * nu;
     }
+    acc16_flush<M, P, ODD>(a, pend);
     RowSums out = {0, 0, 0, 0, 0, 0, 0};
     if (M) {
         out.t2r = a.p2r - (uint64_t)(int64_t)a.eri;
@@ -701,21 +720,6 @@ __device__ __forceinline__ double scaled_mean(uint64_t units, int shift, double 
     return __ddiv_rn(__dmul_rn((double)units, scale), n);
 }
 
-__device__ __forceinline__ Agg load_agg(const Agg *a)
-{
-    const uint4 *v = reinterpret_cast<const uint4 *>(a);
-    const uint4 w0 = __ldcg(v), w1 = __ldcg(v + 1), w2 = __ldcg(v + 2);
-    Agg g;
-    g.s2[0] = ((uint64_t)w0.y << 32) | w0.x;
-    g.s2[1] = ((uint64_t)w0.w << 32) | w0.z;
-    g.s1[0] = ((uint64_t)w1.y << 32) | w1.x;
-    g.s1[1] = ((uint64_t)w1.w << 32) | w1.z;
-    g.psnr = ((uint64_t)w2.y << 32) | w2.x;
-    g.odd = ((uint64_t)w2.w << 32) | w2.z;
-    g.count = g.pad = 0;
-    return g;
-}
-
 __device__ __forceinline__ void store_agg(Agg *a, const Agg &g)
 {
     uint4 *v = reinterpret_cast<uint4 *>(a);
@@ -729,32 +733,6 @@ __device__ __forceinline__ void store_agg(Agg *a, const Agg &g)
 
 __device__ __forceinline__ Agg agg_zero() { return Agg{{0, 0}, {0, 0}, 0, 0, 0, 0}; }
 
-__device__ __forceinline__ Agg agg_add(const Agg &a, const Agg &b)
-{
-    return Agg{{a.s2[0] + b.s2[0], a.s2[1] + b.s2[1]},
-               {a.s1[0] + b.s1[0], a.s1[1] + b.s1[1]},
-               a.psnr + b.psnr,
-               a.odd + b.odd,
-               0,
-               0};
-}
-
-__device__ __forceinline__ Agg warp_sum_agg(Agg a)
-{
-    a.s2[0] = warp_sum(a.s2[0]);
-    a.s2[1] = warp_sum(a.s2[1]);
-    a.s1[0] = warp_sum(a.s1[0]);
-    a.s1[1] = warp_sum(a.s1[1]);
-    a.psnr = warp_sum(a.psnr);
-    a.odd = warp_sum(a.odd);
-    return a;
-}
-
-__device__ __forceinline__ SC agg_sc(const Agg &a, int X)
-{
-    return SC{a.s2[X], X ? (a.odd >> 32) : (a.odd & 0xffffffffull)};
-}
-
 // Items a block of frame blocks holds.
 __device__ __forceinline__ uint64_t block_items(const Params &p, int b)
 {
@@ -762,8 +740,9 @@ __device__ __forceinline__ uint64_t block_items(const Params &p, int b)
 }
 
 // Waits (bounded) until every block of frame f counts all its items, then
-// returns the frame's sums.
-__device__ Agg frame_totals(const Params &p, int f)
+// returns the frame's sums that part `part` needs: plane X's second- and
+// first-moment sums and odd terms (X = part < 2), or the psnr sum.
+__device__ Agg frame_totals(const Params &p, int f, int part)
 {
     const int lane = lane_id(), NB = p.blocks_per_frame;
     const Agg *bl = p.blocks + (size_t)f * NB;
@@ -776,64 +755,121 @@ __device__ Agg frame_totals(const Params &p, int f)
             if (lane == 0) atomicOr(p.status, 1u);
             break;
         }
-        __nanosleep(256);
+        __nanosleep(128);
     }
     Agg t = agg_zero();
-#pragma unroll 4
-    for (int i = lane; i < NB; i += 32) t = agg_add(t, load_agg(bl + i));
-    return warp_sum_agg(t);
+    if (part < 2) {
+        const int X = part;
+        uint64_t s2 = 0, s1 = 0, odd = 0;
+        for (int b = lane; b < NB; b += 32) {
+            s2 += __ldcg(&bl[b].s2[X]);
+            s1 += __ldcg(&bl[b].s1[X]);
+            odd += __ldcg(&bl[b].odd);
+        }
+        t.s2[X] = warp_sum(s2);
+        t.s1[X] = warp_sum(s1);
+        t.odd = warp_sum(odd);
+    } else {
+        uint64_t ps = 0;
+        for (int b = lane; b < NB; b += 32) ps += __ldcg(&bl[b].psnr);
+        t.psnr = warp_sum(ps);
+    }
+    return t;
 }
 
-// The first block of frame f whose inclusive exact prefix of plane X passes
-// 2^53, found as soon as the blocks up to it are complete (later blocks may
-// still be running); NB when the whole frame stays at or below 2^53. Waits
-// (bounded) while a block before the crossing is incomplete. *before gets
-// the prefix (sum, odd terms) before the block returned.
-__device__ int crossing_block(const Params &p, int f, int X, SC *before)
+// A window of up to 32 consecutive aggregates, lane i holding element i and
+// whether it is complete: the first lane not complete (32 if none), the sum
+// of the complete prefix, and the first lane of that prefix whose inclusive
+// prefix from `run` passes 2^53 (-1 if none) with the prefix before it.
+struct WindowScan {
+    int first_open, hit;
+    SC before, tot;
+};
+
+__device__ WindowScan scan_window(bool done, SC v, SC run)
 {
-    const int lane = lane_id(), NB = p.blocks_per_frame;
+    WindowScan w;
+    const int lane = lane_id();
+    const unsigned open = __ballot_sync(kFull, !done);
+    w.first_open = open ? __ffs(open) - 1 : 32;
+    if (lane >= w.first_open) v = SC{0, 0};
+    const SC ex = warp_excl_sc(v, &w.tot);
+    const unsigned hit = __ballot_sync(kFull, lane < w.first_open && run.s + ex.s + v.s > kTwo53);
+    w.hit = hit ? __ffs(hit) - 1 : -1;
+    w.before = sc_add(run, shfl_sc(ex, w.hit >= 0 ? w.hit : 0));
+    return w;
+}
+
+// The first item of frame f whose inclusive exact prefix of plane X passes
+// 2^53, found as soon as the items up to it are complete (later items may
+// still be running); I when the whole frame stays at or below 2^53. Complete
+// blocks are summed from their block sums (the prefix is kept; each poll
+// looks at the 32 blocks from the first incomplete one), the first
+// incomplete block item by item: an item is complete once it carries this
+// launch's stamp. A wait on one block is bounded. *before gets the prefix
+// (sum, odd terms) before the item returned.
+__device__ int crossing_item(const Params &p, int f, int X, SC *before)
+{
+    const int lane = lane_id(), NB = p.blocks_per_frame, I = p.items_per_frame;
     const Agg *bl = p.blocks + (size_t)f * NB;
+    const Agg *it = p.items + (size_t)f * I;
     const int shift = X ? 32 : 0;
+    const auto sums = [X, shift](const Agg *a) {
+        return SC{__ldcg(&a->s2[X]), (__ldcg(&a->odd) >> shift) & 0xffffffffull};
+    };
+    SC run{0, 0};  // exact prefix of blocks [0, base), all complete
+    int base = 0;
     uint32_t spins = 0;
-    for (;;) {
-        SC run{0, 0};
-        bool ready = true;
-        for (int base = 0; base < NB; base += 32) {
-            count(p.ctrl, kCtrlPasses, 1);
-            const int b = base + lane;
-            bool done = true;
-            SC v{0, 0};
-            if (b < NB) {
-                done = ld_acquire64(&bl[b].count) >= block_items(p, b);
-                if (done) v = SC{__ldcg(&bl[b].s2[X]), (__ldcg(&bl[b].odd) >> shift) & 0xffffffffull};
+    while (base < NB) {
+        count(p.ctrl, kCtrlPasses, 1);
+        const int b = base + lane;
+        bool done = true;
+        SC v{0, 0};
+        if (b < NB) {
+            done = ld_acquire64(&bl[b].count) >= block_items(p, b);
+            if (done) v = sums(bl + b);
+        }
+        const WindowScan w = scan_window(done, v, run);
+        if (w.hit >= 0) {  // a complete block: every item in it is out
+            const int i = (base + w.hit) * kBlockItems + lane;
+            const WindowScan wi = scan_window(true, i < I ? sums(it + i) : SC{0, 0}, w.before);
+            *before = wi.before;
+            return (base + w.hit) * kBlockItems + wi.hit;
+        }
+        run = sc_add(run, w.tot);
+        base += w.first_open;
+        if (w.first_open > 0) continue;
+        // Block `base` is incomplete: poll its items alone until the
+        // crossing shows among its complete ones or all of them are out.
+        const int i = base * kBlockItems + lane;
+        const int n = (int)block_items(p, base);
+        for (;;) {
+            bool di = true;
+            SC vi{0, 0};
+            if (lane < n) {
+                di = ld_acquire64(&it[i].count) == p.launch;
+                if (di) vi = sums(it + i);
             }
-            const unsigned open = __ballot_sync(kFull, !done);
-            SC tot;
-            const SC ex = warp_excl_sc(v, &tot);
-            const unsigned hit = __ballot_sync(kFull, b < NB && done && run.s + ex.s + v.s > kTwo53);
-            const int first_open = open ? __ffs(open) - 1 : 32;
-            const int first_hit = hit ? __ffs(hit) - 1 : 32;
-            if (first_hit < first_open) {
-                *before = sc_add(run, shfl_sc(ex, first_hit));
-                return base + first_hit;
+            const WindowScan wi = scan_window(di, vi, run);
+            if (wi.hit >= 0) {
+                *before = wi.before;
+                return base * kBlockItems + wi.hit;
             }
-            if (first_open < 32) {
-                ready = false;
+            if (wi.first_open == 32) {  // the whole block is out
+                run = sc_add(run, wi.tot);
+                ++base;
                 break;
             }
-            run = sc_add(run, tot);
+            if (++spins > p.spin_limit) {  // an item never completed
+                if (lane == 0) atomicOr(p.status, 1u);
+                *before = run;
+                return I;
+            }
+            __nanosleep(64);
         }
-        if (ready) {
-            *before = run;
-            return NB;
-        }
-        if (++spins > p.spin_limit) {
-            if (lane == 0) atomicOr(p.status, 1u);
-            *before = run;
-            return NB;
-        }
-        __nanosleep(256);
     }
+    *before = run;
+    return I;
 }
 
 // S after a run of terms with exact sum and odd count x, in the regime S is
@@ -846,6 +882,54 @@ __device__ __forceinline__ uint64_t regime_after(uint64_t S, SC x, bool exact, i
 __device__ __forceinline__ bool regime_left(uint64_t v, bool exact, int b)
 {
     return exact ? v > kTwo53 : v >= (2ull << b);
+}
+
+// Zeroes the samples of V (64 consecutive samples from j0) before pos; a zero
+// sample adds nothing.
+__device__ __forceinline__ void mask_before(uint4 (&V)[8], int j0, int pos)
+{
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        uint32_t w[4] = {V[v].x, V[v].y, V[v].z, V[v].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = j0 + v * 8 + 2 * q;
+            w[q] &= (j >= pos ? 0x0000ffffu : 0u) | (j + 1 >= pos ? 0xffff0000u : 0u);
+        }
+        V[v] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// The exact sum and the odd-term count of the binary32 squares of 64
+// samples, by the row pass's arithmetic: byte-split dot products for the
+// squares, rounding errors in binary32, odd terms four at a time.
+__device__ __forceinline__ void sums64(const uint4 (&V)[8], uint64_t *sum, uint32_t *odd)
+{
+    uint32_t lo_sum = 0, hi_sum = 0, ob = 0;
+    float2 e = make_float2(0.0f, 0.0f);
+    const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        const uint32_t w[4] = {V[v].x, V[v].y, V[v].z, V[v].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t x = __byte_perm(w[q], 0, 0x3120);
+            lo_sum = __dp2a_lo(w[q], x, lo_sum);
+            hi_sum = __dp2a_hi(w[q], x, hi_sum);
+            const uint32_t g0 = __byte_perm(w[q], kA, 0x7610), g1 = __byte_perm(w[q], kA, 0x7632);
+            const float2 f = __fadd2_rn(make_float2(__uint_as_float(g0), __uint_as_float(g1)), m23);
+            e = __fadd2_rn(e, __ffma2_rn(f, f, neg2(__fmul2_rn(f, f))));
+        }
+#pragma unroll
+        for (int q = 0; q < 4; q += 2) {
+            const uint32_t lo = __byte_perm(w[q], w[q + 1], 0x6420);
+            const uint32_t hi = __byte_perm(w[q], w[q + 1], 0x7531);
+            const uint32_t big = ((hi & 0x7F7F7F7Fu) + 0x70707070u) | hi;  // bit 7: byte >= 16
+            ob += lo & ~(big >> 7) & 0x01010101u;
+        }
+    }
+    *sum = ((uint64_t)hi_sum << 8) + lo_sum - (uint64_t)(int64_t)small_f_to_i(__fadd_rn(e.x, e.y));
+    *odd = (ob & 0xffu) + ((ob >> 8) & 0xffu) + ((ob >> 16) & 0xffu) + (ob >> 24);
 }
 
 // The terms of a 16-bit row starting on a 16-byte boundary, added to S from
@@ -869,21 +953,10 @@ __device__ uint64_t resolve_row_fast(const unsigned char *row, int width, uint64
         uint4 V[8];
 #pragma unroll
         for (int v = 0; v < 8; ++v) V[v] = load_vec<uint16_t, true>(row, (j0 >> 3) + v, width);
-        uint64_t ls = 0;
-        uint32_t lc32 = 0;  // at most 64: a 32-bit count keeps the chains short
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-            const uint32_t w4[4] = {V[v].x, V[v].y, V[v].z, V[v].w};
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int j = j0 + v * 8 + k;
-                const uint32_t t = (j >= pos && j < width)
-                                       ? term_of_sample((w4[k >> 1] >> (16 * (k & 1))) & 0xffffu)
-                                       : 0u;
-                ls += t;
-                lc32 += t & 1u;
-            }
-        }
+        if (j0 < pos) mask_before(V, j0, pos);  // terms before pos are already in S
+        uint64_t ls;
+        uint32_t lc32;
+        sums64(V, &ls, &lc32);
         const uint64_t lc = lc32;
         SC tot;
         const SC ex = warp_excl_sc(SC{ls, lc}, &tot);
@@ -957,31 +1030,24 @@ template <typename TS, bool VEC, bool FULL>
 __device__ uint64_t walk_plane_fast(const Params &p, int f, int X, Agg *t)
 {
     const int I = p.items_per_frame, H = p.height;
-    const Agg *items = p.items + (size_t)f * I;
     const size_t off = ((size_t)f * 2 + X) * H;
     const uint64_t *R = p.s2_rows + off;
     const uint32_t *O = p.odd_rows + off;
-    const uint64_t hi_mask = X ? 32 : 0;
-    SC b0;
-    const int blk = crossing_block(p, f, X, &b0);
-    if (blk >= p.blocks_per_frame) {
-        *t = frame_totals(p, f);
+    SC pre_items;
+    const int it = crossing_item(p, f, X, &pre_items);
+    if (it >= I) {
+        *t = frame_totals(p, f, X);
         count(p.ctrl, kCtrlRowsExact, (uint32_t)H);
         return t->s2[X];
     }
-    SC b1;
-    const int it = warp_first(
-        [items, X, hi_mask](int i) {
-            return SC{__ldcg(&items[i].s2[X]), (__ldcg(&items[i].odd) >> hi_mask) & 0xffffffffull};
-        },
-        blk * kBlockItems, min(I, (blk + 1) * kBlockItems),
-        [b0](SC x) { return b0.s + x.s > kTwo53; }, &b1, p.ctrl);
-    const SC pre_items = sc_add(b0, b1);
-    SC b2;
+    SC b2{0, 0};
     const int r0 = it * p.rows_per_item;
-    const int row = warp_first([R, O](int i) { return SC{__ldcg(R + i), (uint64_t)__ldcg(O + i)}; },
-                               r0, min(H, r0 + p.rows_per_item),
-                               [pre_items](SC x) { return pre_items.s + x.s > kTwo53; }, &b2, p.ctrl);
+    const int row = p.rows_per_item == 1  // the item is the row
+                        ? r0
+                        : warp_first([R, O](int i) { return SC{__ldcg(R + i), (uint64_t)__ldcg(O + i)}; },
+                                     r0, min(H, r0 + p.rows_per_item),
+                                     [pre_items](SC x) { return pre_items.s + x.s > kTwo53; }, &b2,
+                                     p.ctrl);
     const SC pre = sc_add(pre_items, b2);
     count(p.ctrl, kCtrlRowsExact, (uint32_t)row);
     const unsigned char *plane = (X == 0 ? p.ref : p.dis) + (int64_t)f * p.pitch;
@@ -991,7 +1057,7 @@ __device__ uint64_t walk_plane_fast(const Params &p, int f, int X, Agg *t)
     else S = resolve_row<TS>(rp, p.width, S, p.ctrl);
     count(p.ctrl, kCtrlRowsTerms, 1);
     const uint64_t rs = __ldcg(R + row), rc = __ldcg(O + row);
-    *t = frame_totals(p, f);
+    *t = frame_totals(p, f, X);
     const uint64_t tot = t->s2[X], tot_odd = X ? (t->odd >> 32) : (t->odd & 0xffffffffull);
     const uint64_t rest_s = tot - pre.s - rs, rest_c = tot_odd - pre.c - rc;
     if (S >= kTwo53 && binade_of(S) <= 54) {
@@ -1019,7 +1085,7 @@ __device__ __noinline__ void walk_part(const Params &p, int f, int part)
         if (ODD) {
             s2 = walk_plane_fast<TS, VEC, FULL>(p, f, X, &t);
         } else {  // such frames stay at or below 2^53 units
-            t = frame_totals(p, f);
+            t = frame_totals(p, f, X);
             s2 = t.s2[X];
             count(p.ctrl, kCtrlRowsExact, (uint32_t)p.height);
         }
@@ -1029,7 +1095,7 @@ __device__ __noinline__ void walk_part(const Params &p, int f, int part)
             if (p.s2_sums) p.s2_sums[(size_t)f * 2 + X] = s2;
         }
     } else if (P) {
-        const Agg t = frame_totals(p, f);
+        const Agg t = frame_totals(p, f, 2);
         const uint64_t d = t.psnr <= kTwo53 ? t.psnr
                                             : walk_rows(p.psnr_rows + (size_t)f * p.height, p.height, p.ctrl);
         if (lead) {
@@ -1083,6 +1149,29 @@ __device__ __noinline__ void lookback(const Params &p, int f, int j, uint64_t ag
     *pre_d = pd;
 }
 
+// The order items are handed out in: frame by frame, except that the last
+// kTailFrames frames (all of them in a batch of at most that many) go row by
+// row across those frames. A frame's crossing row (about three quarters down
+// a frame of uniform noise) is then out well before the batch's last rows,
+// so its walk runs while they stream instead of after them.
+#ifndef VMX_TAIL_FRAMES
+#define VMX_TAIL_FRAMES 16
+#endif
+constexpr int kTailFrames = VMX_TAIL_FRAMES;
+__device__ __forceinline__ void item_of_ticket(int tk, int F, int I, int *f, int *j)
+{
+    const int K = min(F, kTailFrames);
+    const int head = (F - K) * I;
+    if (tk < head) {
+        *f = tk / I;
+        *j = tk - *f * I;
+    } else {
+        const int t = tk - head;
+        *j = t / K;
+        *f = F - K + (t - *j * K);
+    }
+}
+
 template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
 {
@@ -1116,7 +1205,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         }
         const int tk = (int)cur++;
         if (tk >= nitems) break;
-        const int f = tk / I, j = tk - f * I;
+        int f, j;
+        item_of_ticket(tk, p.frames, I, &f, &j);
         const int r0 = j * p.rows_per_item, r1 = min(H, r0 + p.rows_per_item);
         const unsigned char *fr = p.ref + (int64_t)f * p.pitch;
         const unsigned char *fd = p.dis + (int64_t)f * p.pitch;
@@ -1150,16 +1240,24 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
                 my_o = (uint64_t)rs.oddr | ((uint64_t)rs.oddd << 32);
             }
         }
+        // Lane 0 alone stores and adds the item's sums: a one-row item has
+        // them in lane 0 already. First-moment sums of an item fit 32 bits
+        // (at most 32768 samples below 2^16).
         Agg g = agg_zero();
+        const bool one = r1 - r0 == 1;
         if (M) {
-            g.s2[0] = warp_sum(my_r);
-            g.s2[1] = warp_sum(my_d);
-            g.s1[0] = warp_sum((uint64_t)s1r);
-            g.s1[1] = warp_sum((uint64_t)s1d);
+            g.s2[0] = one ? my_r : warp_sum(my_r);
+            g.s2[1] = one ? my_d : warp_sum(my_d);
+            g.s1[0] = warp_sum32(s1r);
+            g.s1[1] = warp_sum32(s1d);
         }
-        if (ODD) g.odd = warp_sum(my_o);
-        if (P) g.psnr = warp_sum(my_p);
-        if (lane == 0) store_agg(p.items + (size_t)f * I + j, g);
+        if (ODD) g.odd = one ? my_o : warp_sum(my_o);
+        if (P) g.psnr = one ? my_p : warp_sum(my_p);
+        if (lane == 0) {
+            Agg *ia = p.items + (size_t)f * I + j;
+            store_agg(ia, g);
+            st_release64(&ia->count, p.launch);  // the item's sums are out
+        }
 
         // B. frames that can pass 2^55: runs of the rows planned from 55 up.
         if (FULL && M) {
