@@ -1109,42 +1109,56 @@ __device__ __noinline__ void walk_part(const Params &p, int f, int part)
 
 // The exact second-moment sums of the frame's items before item j, by a
 // decoupled look-back over flags (1: the item's own sums are out, 2: the
-// inclusive sums are out). Called by one lane. A wait longer than
-// p.spin_limit polls sets the status word and gives up.
+// inclusive sums are out), 32 predecessors at a time: the flag-1 sums up to
+// the nearest inclusive prefix are added at once; a nearer item with nothing
+// out yet is waited for. Called by the whole warp; lane 0's aggr, aggd are
+// the item's own sums. A wait longer than p.spin_limit polls sets the status
+// word and gives up.
 __device__ __noinline__ void lookback(const Params &p, int f, int j, uint64_t aggr, uint64_t aggd,
                                       uint64_t *pre_r, uint64_t *pre_d)
 {
+    const int lane = lane_id();
     const size_t base = (size_t)f * p.items_per_frame;
     const size_t idx = base + j;
     uint64_t pr = 0, pd = 0;
     if (j > 0) {
-        st_release(p.flags + idx, 1u);  // the item's sums were written before the fence
+        if (lane == 0) st_release(p.flags + idx, 1u);  // the item's sums were stored before
         int q = j - 1;
         uint32_t spins = 0;
         for (;;) {
-            const uint32_t fl = ld_acquire(p.flags + base + q);
-            if (fl == 2u) {
-                pr += __ldcg(p.item_inc + (base + q) * 2);
-                pd += __ldcg(p.item_inc + (base + q) * 2 + 1);
-                break;
-            }
-            if (fl == 1u) {
-                pr += __ldcg(&p.items[base + q].s2[0]);
-                pd += __ldcg(&p.items[base + q].s2[1]);
-                --q;  // item 0 always publishes 2, so q stays >= 0
+            const int i = q - lane;  // lane 0 the nearest predecessor
+            const uint32_t fl = i >= 0 ? ld_acquire(p.flags + base + i) : 2u;
+            const unsigned zero = __ballot_sync(kFull, fl == 0u);
+            const unsigned incl = __ballot_sync(kFull, fl == 2u);
+            const int fz = zero ? __ffs(zero) - 1 : 32;
+            const int fi = incl ? __ffs(incl) - 1 : 32;
+            if (fz < fi) {
+                if (++spins > p.spin_limit) {
+                    if (lane == 0) atomicOr(p.status, 1u);
+                    break;
+                }
+                __nanosleep(64);
                 continue;
             }
-            if (++spins > p.spin_limit) {
-                atomicOr(p.status, 1u);
-                break;
+            uint64_t vr = 0, vd = 0;
+            if (i >= 0 && lane < fi) {
+                vr = __ldcg(&p.items[base + i].s2[0]);
+                vd = __ldcg(&p.items[base + i].s2[1]);
+            } else if (i >= 0 && lane == fi) {
+                vr = __ldcg(p.item_inc + (base + i) * 2);
+                vd = __ldcg(p.item_inc + (base + i) * 2 + 1);
             }
-            __nanosleep(64);
+            pr += warp_sum(vr);
+            pd += warp_sum(vd);
+            if (fi < 32) break;  // an inclusive prefix (item 0 always publishes one)
+            q -= 32;
         }
     }
-    __stcg(p.item_inc + idx * 2, pr + aggr);
-    __stcg(p.item_inc + idx * 2 + 1, pd + aggd);
-    __threadfence();
-    st_release(p.flags + idx, 2u);
+    if (lane == 0) {
+        __stcg(p.item_inc + idx * 2, pr + aggr);
+        __stcg(p.item_inc + idx * 2 + 1, pd + aggd);
+        st_release(p.flags + idx, 2u);
+    }
     *pre_r = pr;
     *pre_d = pd;
 }
@@ -1262,12 +1276,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         // B. frames that can pass 2^55: runs of the rows planned from 55 up.
         if (FULL && M) {
             uint64_t pr = 0, pd = 0;
-            if (lane == 0) {
-                __threadfence();
-                lookback(p, f, j, g.s2[0], g.s2[1], &pr, &pd);
-            }
-            pr = __shfl_sync(kFull, pr, 0);
-            pd = __shfl_sync(kFull, pd, 0);
+            lookback(p, f, j, g.s2[0], g.s2[1], &pr, &pd);
             for (int X = 0; X < 2; ++X) {
                 const uint64_t pre = X ? pd : pr;
                 const uint64_t mine = X ? my_d : my_r;
