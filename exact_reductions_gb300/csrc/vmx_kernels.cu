@@ -220,16 +220,16 @@ struct RowSums {
 // Odd terms: a binary32 square of a codeword is odd exactly when the codeword
 // is odd and below 4096, i.e. its low byte is odd and its high byte below 16;
 // four samples (two per plane) are tested at once in byte lanes.
-// First moments: integer sums of g, less the 2^23 bias.
+// First moments: integer sums of g over the row, the 2^23 bias taken off at
+// the row's end (the true sums fit 32 bits, so the wrap-around is harmless).
+// Each flush folds its rounding errors into the row's term sums at once.
 struct Acc16 {
     uint32_t lr, hr, ld, hd, lx, hx;  // dot-product sums since the last flush
-    uint32_t gsr, gsd;                // sums of g since the last flush
     uint32_t oddb;                    // odd terms since the last flush, one byte per sample slot
     float2 er, ed, ep;                // rounding errors since the last flush
-    uint64_t p2r, p2d, px;            // row sums of p^2, q^2, p q
-    uint32_t s1r, s1d, odd;           // row sums of p, q; odd terms (ref low half, dis high)
-    int32_t eri, edi, epi;            // row sums of the rounding errors
-    uint64_t dd;                      // psnr alone: row sum of d^2
+    uint32_t gsr, gsd;                // row sums of g
+    uint32_t odd;                     // row's odd terms (ref low half, dis high)
+    uint64_t t2r, t2d, tp;            // row sums of the terms: squares of p, of q, of d
 };
 
 __device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
@@ -265,43 +265,42 @@ __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
     if (P) {
         const float2 x = __fadd2_rn(fr, neg2(fd));  // exact
         a.ep = __fadd2_rn(a.ep, __ffma2_rn(x, x, neg2(__fmul2_rn(x, x))));
-        if (!M) {
+        if (!M) {  // psnr alone: d^2 from the signed difference, straight into the row sum
             const int32_t i0 = (int32_t)(gr0 - gd0), i1 = (int32_t)(gr1 - gd1);
-            a.dd += (uint64_t)((int64_t)i0 * i0);
-            a.dd += (uint64_t)((int64_t)i1 * i1);
+            a.tp += (uint64_t)((int64_t)i0 * i0);
+            a.tp += (uint64_t)((int64_t)i1 * i1);
         }
     }
 }
 
-// Moves one iteration's sums to the row sums. `slots` samples per plane went
-// into them: at most 64 per lane keeps every 32-bit sum below 2^30 (64 times
-// 65535 times 255), every error sum below 2^13 and every odd-term byte below
-// 2^8.
+// Folds the sums since the last flush into the row sums. At most 64 samples
+// per lane and plane since the last flush keep every 32-bit sum below 2^30
+// (64 times 65535 times 255), every error sum below 2^13 and every odd-term
+// byte below 2^8.
 template <bool M, bool P, bool ODD>
-__device__ __forceinline__ void acc16_flush(Acc16 &a, uint32_t slots)
+__device__ __forceinline__ void acc16_flush(Acc16 &a)
 {
+    const int64_t ep = P ? small_f_to_i(__fadd_rn(a.ep.x, a.ep.y)) : 0;
     if (M) {
-        a.s1r += a.gsr - slots * kA;
-        a.s1d += a.gsd - slots * kA;
-        a.p2r += ((uint64_t)a.hr << 8) + a.lr;
-        a.p2d += ((uint64_t)a.hd << 8) + a.ld;
-        a.eri += small_f_to_i(__fadd_rn(a.er.x, a.er.y));
-        a.edi += small_f_to_i(__fadd_rn(a.ed.x, a.ed.y));
-        a.lr = a.hr = a.ld = a.hd = a.gsr = a.gsd = 0;
-        a.er = a.ed = make_float2(0.0f, 0.0f);
+        const uint64_t pr = ((uint64_t)a.hr << 8) + a.lr;  // sums of p^2, q^2
+        const uint64_t pd = ((uint64_t)a.hd << 8) + a.ld;
+        a.t2r += pr - (uint64_t)(int64_t)small_f_to_i(__fadd_rn(a.er.x, a.er.y));
+        a.t2d += pd - (uint64_t)(int64_t)small_f_to_i(__fadd_rn(a.ed.x, a.ed.y));
         if (P) {
-            a.px += ((uint64_t)a.hx << 8) + a.lx;
+            const uint64_t px = ((uint64_t)a.hx << 8) + a.lx;  // sum of p q
+            a.tp += pr + pd - 2ull * px - (uint64_t)ep;
             a.lx = a.hx = 0;
         }
+        a.lr = a.hr = a.ld = a.hd = 0;
+        a.er = a.ed = make_float2(0.0f, 0.0f);
         if (ODD) {
             a.odd += (a.oddb & 0x00FF00FFu) + ((a.oddb >> 8) & 0x00FF00FFu);
             a.oddb = 0;
         }
+    } else if (P) {
+        a.tp -= (uint64_t)ep;
     }
-    if (P) {
-        a.epi += small_f_to_i(__fadd_rn(a.ep.x, a.ep.y));
-        a.ep = make_float2(0.0f, 0.0f);
-    }
+    if (P) a.ep = make_float2(0.0f, 0.0f);
 }
 
 template <bool M, bool P, bool ODD, bool VEC>
@@ -317,7 +316,7 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
         // but at the row's end, where vectors past it are skipped.
         const int nu = min(kUnroll, (nvt - base + 31) >> 5);
         if (pend + 8 * nu > 64) {
-            acc16_flush<M, P, ODD>(a, pend);
+            acc16_flush<M, P, ODD>(a);
             pend = 0;
         }
         uint4 R[kUnroll], D[kUnroll];
@@ -340,18 +339,16 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
         }
         pend += 8 * nu;
     }
-    acc16_flush<M, P, ODD>(a, pend);
+    acc16_flush<M, P, ODD>(a);
     RowSums out = {0, 0, 0, 0, 0, 0, 0};
     if (M) {
-        out.t2r = a.p2r - (uint64_t)(int64_t)a.eri;
-        out.t2d = a.p2d - (uint64_t)(int64_t)a.edi;
-        out.s1r = a.s1r;
-        out.s1d = a.s1d;
+        const uint32_t n = 8u * (uint32_t)((nvt + 31) >> 5);  // samples per lane, zeros included
+        out.t2r = a.t2r;
+        out.t2d = a.t2d;
+        out.s1r = a.gsr - n * kA;
+        out.s1d = a.gsd - n * kA;
     }
-    if (P) {
-        const uint64_t d2 = M ? a.p2r + a.p2d - 2ull * a.px : a.dd;  // sum d^2
-        out.tp = d2 - (uint64_t)(int64_t)a.epi;
-    }
+    if (P) out.tp = a.tp;
     // Row totals; the first-moment sums stay per lane (the item adds them).
     out.t2r = warp_sum(out.t2r);
     out.t2d = warp_sum(out.t2d);
