@@ -1199,6 +1199,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
     // would run one after another. Waits stay deadlock-free: a warp works
     // through its chunk in order, so the smallest unfinished item is always
     // some warp's current item.
+    __shared__ ulonglong4 item_rows[kWarps][kMaxRowsPerItem];  // sums of an item's rows
+    const int wid = (int)(threadIdx.x >> 5);
     const uint32_t nwarps = gridDim.x * (uint32_t)kWarps;
     const uint32_t gwarp = blockIdx.x * (uint32_t)kWarps + (threadIdx.x >> 5);
     const uint32_t first = FULL ? 0u : nwarps;  // tickets below are assigned
@@ -1222,10 +1224,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         const unsigned char *fr = p.ref + (int64_t)f * p.pitch;
         const unsigned char *fd = p.dis + (int64_t)f * p.pitch;
 
-        // A. exact row sums. Lane 0 records each row; lane i keeps the sums
-        // of the item's row i, so that no item totals stay live across rows.
+        // A. exact row sums. Lane 0 records each row and keeps its sums in
+        // the warp's shared slots, so that no item totals stay live in
+        // registers across rows; lane i reads row i's back afterwards.
         uint32_t s1r = 0, s1d = 0;  // this lane's first-moment sums
-        uint64_t my_r = 0, my_d = 0, my_p = 0, my_o = 0;
         for (int r = r0; r < r1; ++r) {
             const unsigned char *rr = fr + (int64_t)r * p.stride;
             const unsigned char *dr = fd + (int64_t)r * p.stride;
@@ -1244,13 +1246,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
             }
             s1r += (uint32_t)rs.s1r;
             s1d += (uint32_t)rs.s1d;
-            if (lane == r - r0) {
-                my_r = rs.t2r;
-                my_d = rs.t2d;
-                my_p = rs.tp;
-                my_o = (uint64_t)rs.oddr | ((uint64_t)rs.oddd << 32);
-            }
+            if (lane == 0) item_rows[wid][r - r0] = make_ulonglong4(rs.t2r, rs.t2d, rs.tp,
+                                                                    (uint64_t)rs.oddr | ((uint64_t)rs.oddd << 32));
         }
+        __syncwarp();
+        uint64_t my_r = 0, my_d = 0, my_p = 0, my_o = 0;  // this lane's row of the item
+        if (lane < r1 - r0) {
+            const ulonglong4 v = item_rows[wid][lane];
+            my_r = v.x;
+            my_d = v.y;
+            my_p = v.z;
+            my_o = v.w;
+        }
+        __syncwarp();
         // Lane 0 alone stores and adds the item's sums: a one-row item has
         // them in lane 0 already. First-moment sums of an item fit 32 bits
         // (at most 32768 samples below 2^16).
