@@ -23,7 +23,7 @@ constexpr int kMinBlocks = VMX_MIN_BLOCKS; // CTAs per SM the kernel is compiled
 constexpr int kMaxRowsPerItem = 32;        // rows per item, at most
 constexpr int kMaxChunk = 4;               // items a warp takes per ticket, at most
 #ifndef VMX_ITEM_PIXELS
-#define VMX_ITEM_PIXELS 2048
+#define VMX_ITEM_PIXELS 4096
 #endif
 constexpr int kItemPixels = VMX_ITEM_PIXELS; // target pixels per warp item
 constexpr int kUnroll = VMX_UNROLL;        // 16-byte vectors in flight per lane per plane
