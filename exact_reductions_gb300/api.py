@@ -118,6 +118,37 @@ def frames(ref: torch.Tensor, dis: torch.Tensor, bpc: int, features: int = 3,
     return out
 
 
+class FrameGraph:
+    """One call of ``frames`` on fixed device tensors, captured as a CUDA graph.
+
+    For a stream of batches of one shape: the inputs are read from ``ref`` and
+    ``dis`` (copy each new batch into them), the outputs land in
+    ``self.out`` and the workspace is fixed; ``replay()`` enqueues the
+    control-word clear and the frame kernel on the current stream as one
+    graph launch, with less launch overhead than separate calls. Bounded
+    device waits that give up are reported by ``status()``."""
+
+    def __init__(self, ref: torch.Tensor, dis: torch.Tensor, bpc: int, features: int = 3,
+                 width: Optional[int] = None, s2_rows: bool = False, sums: bool = False):
+        first = frames(ref, dis, bpc, features, width, s2_rows, sums)  # loads the kernels
+        self.ws = first["_workspace"]
+        side = torch.cuda.Stream(device=ref.device)
+        side.wait_stream(torch.cuda.current_stream(ref.device))
+        with torch.cuda.stream(side):
+            frames(ref, dis, bpc, features, width, s2_rows, sums, ws=self.ws)
+        torch.cuda.current_stream(ref.device).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.out = frames(ref, dis, bpc, features, width, s2_rows, sums, ws=self.ws)
+
+    def replay(self) -> Dict[str, torch.Tensor]:
+        self.graph.replay()
+        return self.out
+
+    def status(self) -> int:
+        return workspace_status(self.ws)
+
+
 def moment_frames(ref, dis, bpc, **kw) -> Dict[str, torch.Tensor]:
     return frames(ref, dis, bpc, features=_lib.FEATURE_MOMENT, **kw)
 

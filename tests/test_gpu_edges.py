@@ -126,6 +126,31 @@ def test_host_entry_reads_pinned_frames_in_place(chunk):
     assert np.array_equal(pinned["s2_rows"], u64(dev["s2_rows"]))
 
 
+def test_graph_replays_match_calls():
+    """A captured call replayed on new inputs copied into the same tensors
+    gives the plain call's outputs (and the oracle's) every time."""
+    wl = synth.WORKLOADS["T1"]
+    ref, dis = wl.batch(1)
+    rng = np.random.default_rng(11)
+    R, D = to_device(ref), to_device(dis)
+    fg = api.FrameGraph(R, D, 16, s2_rows=True, sums=True)
+    for step in range(3):
+        if step:
+            ref = rng.integers(40000, 65536, size=ref.shape, dtype=np.uint16)
+            R.copy_(torch.from_numpy(ref))
+        out = fg.replay()
+        plain = api.frames(R, D, 16, s2_rows=True, sums=True)
+        torch.cuda.synchronize()
+        assert fg.status() == 0
+        for k in ("moments", "mse"):
+            assert same_doubles(out[k].cpu().numpy(), plain[k].cpu().numpy()), (step, k)
+        for k in ("psnr_rows", "s2_rows", "s2_sums", "noise_sums"):
+            assert np.array_equal(u64(out[k]), u64(plain[k])), (step, k)
+        want = oracle_frames(ref, dis, 16, [0])[0]
+        assert same_doubles(out["moments"].cpu().numpy()[0], want["moments"])
+        assert np.array_equal(u64(out["s2_sums"])[0], want["s2_sums"])
+
+
 def test_launch_counter_counts_calls():
     wl = synth.WORKLOADS["C1"]
     ref, dis = wl.batch()
