@@ -5,9 +5,11 @@ python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
 
 A step is one pass of the whole path (exact row sums, look-back, runs, walk,
 finalisation for both features) over one batch of 16 seeded synthetic frame
-pairs already resident in HBM: one library call (control-word clear + the
-frame kernel) captured once as a CUDA graph and replayed per step
-(api.FrameGraph). The batch (531 MB) is larger than L2. Under
+pairs already resident in HBM: one library call on its own workspace and
+outputs. Steps run as a stream of batches does: CUDA graphs of four calls
+(api.FrameGraph), the workspaces cleared first and each kernel launched to
+overlap the end of the one before it (programmatic dependent launch). The
+batch (531 MB) is larger than L2. Under
 torchrun every rank runs its own batch on its own GPU (frames shard with no
 collective; weak scaling); rank 0 prints one JSON line. ``--impl
 reference`` times the CPU oracle on the host cores instead.
@@ -251,40 +253,43 @@ def run_ours(args, rank, local_rank, world, pg):
     F = ref_h.shape[0]
     ref = torch.from_numpy(ref_h).to(dev)
     dis = torch.from_numpy(dis_h).to(dev)
-    # The step: one fused call on the resident batch, captured once as a CUDA
-    # graph (control-word clear + the frame kernel) and replayed per step.
-    fg = api.FrameGraph(ref, dis, wl.bpc, features=3)
-    ws = fg.ws
+    # The step: one fused call on the resident batch. Steps go in CUDA graphs
+    # of `depth` calls (api.FrameGraph), each kernel launched to overlap the
+    # end of the one before it, as a stream of batches runs; every call does
+    # the whole work on its own workspace and outputs.
+    depth = 4 if args.steps % 4 == 0 else 1
+    fg = api.FrameGraph(ref, dis, wl.bpc, features=3, depth=depth)
     stream = torch.cuda.current_stream(dev)
     kernels_per_step = 1
 
-    def step():
+    def replay():
         return fg.replay()
 
     for _ in range(max(args.warmup, 3)):
-        step()
+        replay()
     torch.cuda.synchronize()
-    assert api.workspace_status(ws) == 0, "bounded device wait gave up"
+    assert fg.status() == 0, "bounded device wait gave up"
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    replays = args.steps // depth
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(replays)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(replays)]
 
     with Clocks(local_rank) as clocks:
         if pg is not None:
             dist.barrier(group=pg)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for i in range(args.steps):
+        for i in range(replays):
             starts[i].record(stream)
-            step()
+            replay()
             ends[i].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         if pg is not None:
             dist.barrier(group=pg)
     launches = kernels_per_step * args.steps  # graph replays: one kernel each
-    assert api.workspace_status(ws) == 0, "bounded device wait gave up"
-    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
+    assert fg.status() == 0, "bounded device wait gave up"
+    per = [s.elapsed_time(e) / depth for s, e in zip(starts, ends)]  # ms per call
     device_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), pg)
     value = whole_job_rate(world, F, args.steps, device_ms / 1e3)
 

@@ -22,6 +22,8 @@ VMX_ESCRATCH = -5
 NOALLOC_SCRATCH_BYTES = 16 << 20
 FEATURE_MOMENT = 1
 FEATURE_PSNR = 2
+FLAG_CLEARED = 1
+FLAG_OVERLAP = 2
 
 # Every symbol include/vmx.h declares: name -> (restype, argtypes).
 _vp, _i32, _i64, _sz, _u64, _dbl = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
@@ -34,6 +36,9 @@ SIGNATURES = {
                                      _sz, _vp]),
     "vmx_moment_psnr_frames": (_i32, [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _vp, _vp, _vp, _vp,
                                       _vp, _vp, _vp, _sz, _vp]),
+    "vmx_workspace_clear": (_i32, [_vp, _sz, _i32, _i32, _i32, _i32, _i32, _vp]),
+    "vmx_frames_ex": (_i32, [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
+                             _vp, _vp, _sz, ctypes.c_uint, _vp]),
     "vmx_workspace_status": (_i32, [_vp, _vp]),
     "vmx_workspace_stats": (_i32, [_vp, _vp, _vp]),
     "vmx_psnr_db": (_i32, [_vp, _i32, _i32, _dbl, _vp]),

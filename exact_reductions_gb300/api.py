@@ -119,34 +119,84 @@ def frames(ref: torch.Tensor, dis: torch.Tensor, bpc: int, features: int = 3,
 
 
 class FrameGraph:
-    """One call of ``frames`` on fixed device tensors, captured as a CUDA graph.
+    """Calls of the fused kernel on fixed device tensors, captured as one CUDA
+    graph, for a stream of batches of one shape.
 
-    For a stream of batches of one shape: the inputs are read from ``ref`` and
-    ``dis`` (copy each new batch into them), the outputs land in
-    ``self.out`` and the workspace is fixed; ``replay()`` enqueues the
-    control-word clear and the frame kernel on the current stream as one
-    graph launch, with less launch overhead than separate calls. Bounded
-    device waits that give up are reported by ``status()``."""
+    ``depth`` batches per replay, each with its own workspace and outputs
+    (``self.outs[i]``; ``self.out`` is the last): the workspaces are cleared
+    first, then the kernels run back to back, each launched to overlap the
+    end of the one before it (``vmx_frames_ex`` with ``VMX_FLAG_OVERLAP``).
+    ``refs``/``diss`` give each batch's input tensors (copy new frames into
+    them between replays); by default every batch reads ``ref``/``dis``.
+    Bounded device waits that give up are reported by ``status()``."""
 
     def __init__(self, ref: torch.Tensor, dis: torch.Tensor, bpc: int, features: int = 3,
-                 width: Optional[int] = None, s2_rows: bool = False, sums: bool = False):
-        first = frames(ref, dis, bpc, features, width, s2_rows, sums)  # loads the kernels
-        self.ws = first["_workspace"]
-        side = torch.cuda.Stream(device=ref.device)
-        side.wait_stream(torch.cuda.current_stream(ref.device))
+                 width: Optional[int] = None, s2_rows: bool = False, sums: bool = False,
+                 depth: int = 1, refs=None, diss=None):
+        lib = _lib.load()
+        refs = list(refs) if refs is not None else [ref] * depth
+        diss = list(diss) if diss is not None else [dis] * depth
+        if len(refs) != depth or len(diss) != depth:
+            raise ValueError("refs and diss need one tensor per batch")
+        geo = [_geometry(r, d, bpc, width) for r, d in zip(refs, diss)]
+        _, _, F, H, W, stride = geo[0]
+        dev = refs[0].device
+        need = int(lib.vmx_workspace_bytes(W, H, bpc, F, features))
+        if need == 0:
+            raise ValueError("shape rejected by libvmx")
+        m = bool(features & _lib.FEATURE_MOMENT)
+        p = bool(features & _lib.FEATURE_PSNR)
+        self.ws = [workspace(need, dev) for _ in range(depth)]
+        self.outs = []
+        for _ in range(depth):
+            o: Dict[str, torch.Tensor] = {}
+            if m:
+                o["moments"] = torch.empty((F, 4), dtype=torch.float64, device=dev)
+                if s2_rows:
+                    o["s2_rows"] = torch.empty((F, 2, H), dtype=torch.uint64, device=dev)
+                if sums:
+                    o["s2_sums"] = torch.empty((F, 2), dtype=torch.uint64, device=dev)
+            if p:
+                o["psnr_rows"] = torch.empty((F, H), dtype=torch.uint64, device=dev)
+                o["mse"] = torch.empty((F,), dtype=torch.float64, device=dev)
+                if sums:
+                    o["noise_sums"] = torch.empty((F,), dtype=torch.uint64, device=dev)
+            self.outs.append(o)
+        self.out = self.outs[-1]
+
+        def enqueue():
+            st = _stream(dev)
+            for w in self.ws:
+                _lib.check(lib.vmx_workspace_clear(w.data_ptr(), w.numel(), W, H, bpc, F,
+                                                   features, st), "vmx workspace_clear")
+            for i, ((r, d, _, _, _, _), o, w) in enumerate(zip(geo, self.outs, self.ws)):
+                flags = _lib.FLAG_CLEARED | (_lib.FLAG_OVERLAP if i else 0)
+                _lib.check(lib.vmx_frames_ex(
+                    r.data_ptr(), d.data_ptr(), W, H, stride, bpc, F, features,
+                    _ptr(o.get("moments")), _ptr(o.get("s2_rows")), _ptr(o.get("s2_sums")),
+                    _ptr(o.get("psnr_rows")), _ptr(o.get("mse")), _ptr(o.get("noise_sums")),
+                    w.data_ptr(), w.numel(), flags, st), "vmx frames_ex")
+
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(side):
-            frames(ref, dis, bpc, features, width, s2_rows, sums, ws=self.ws)
-        torch.cuda.current_stream(ref.device).wait_stream(side)
+            enqueue()  # loads the kernels, outside the capture
+        torch.cuda.current_stream(dev).wait_stream(side)
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
-            self.out = frames(ref, dis, bpc, features, width, s2_rows, sums, ws=self.ws)
+            enqueue()
 
     def replay(self) -> Dict[str, torch.Tensor]:
         self.graph.replay()
         return self.out
 
     def status(self) -> int:
-        return workspace_status(self.ws)
+        """VMX_OK, or the first nonzero status of the batches' workspaces."""
+        for w in self.ws:
+            st = workspace_status(w)
+            if st:
+                return st
+        return 0
 
 
 def moment_frames(ref, dis, bpc, **kw) -> Dict[str, torch.Tensor]:

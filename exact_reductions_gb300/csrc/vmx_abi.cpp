@@ -113,8 +113,11 @@ struct Outputs {
 // workspace's own status word (cleared with the other control words).
 int run_frames(const void *ref, const void *dis, int width, int height, int64_t stride,
                int bpc, int nframes, int features, const Outputs &o, void *workspace,
-               size_t workspace_bytes, cudaStream_t stream, uint32_t *status_word = nullptr)
+               size_t workspace_bytes, cudaStream_t stream, uint32_t *status_word = nullptr,
+               unsigned flags = 0)
 {
+    if (flags & ~(unsigned)(VMX_FLAG_CLEARED | VMX_FLAG_OVERLAP)) return VMX_EINVAL;
+    if (flags && !workspace) return VMX_EINVAL;
     Layout L;
     if (!ref || !dis || !make_layout(width, height, bpc, nframes, features, &L)) return VMX_EINVAL;
     if (stride < (int64_t)width * bytes_per_sample(bpc)) return VMX_EINVAL;
@@ -164,8 +167,10 @@ int run_frames(const void *ref, const void *dis, int width, int height, int64_t 
     p.noise_sums = o.noise_sums;
     p.spin_limit = kSpinLimit;
     p.launch = next_launch_number();
+    p.overlap = (flags & VMX_FLAG_OVERLAP) ? 1u : 0u;
     const bool vec = (uintptr_t)ref % 16 == 0 && (uintptr_t)dis % 16 == 0 && stride % 16 == 0;
-    err = cudaMemsetAsync(ws + L.off_ctrl, 0, L.ctrl_bytes, stream);
+    err = (flags & VMX_FLAG_CLEARED) ? cudaSuccess
+                                     : cudaMemsetAsync(ws + L.off_ctrl, 0, L.ctrl_bytes, stream);
     if (err == cudaSuccess) {
         err = launch_frames(p, L, features, vec, stream);
         if (err == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -245,6 +250,28 @@ int vmx_moment_psnr_frames(const void *ref, const void *dis, int width, int heig
     return run_frames(ref, dis, width, height, stride_bytes, bpc, nframes,
                       VMX_FEATURE_MOMENT | VMX_FEATURE_PSNR, o, workspace, workspace_bytes,
                       static_cast<cudaStream_t>(stream));
+}
+
+int vmx_workspace_clear(void *workspace, size_t workspace_bytes, int width, int height, int bpc,
+                        int nframes, int features, void *stream)
+{
+    Layout L;
+    if (!workspace || !make_layout(width, height, bpc, nframes, features, &L)) return VMX_EINVAL;
+    if (workspace_bytes < L.total || (uintptr_t)workspace % 256) return VMX_EINVAL;
+    const cudaError_t err =
+        cudaMemsetAsync(static_cast<unsigned char *>(workspace) + L.off_ctrl, 0, L.ctrl_bytes,
+                        static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? VMX_OK : cuda_fail(err);
+}
+
+int vmx_frames_ex(const void *ref, const void *dis, int width, int height, int64_t stride_bytes,
+                  int bpc, int nframes, int features, double *moments, uint64_t *s2_rows,
+                  uint64_t *s2_sums, uint64_t *psnr_rows, double *mse, uint64_t *noise_sums,
+                  void *workspace, size_t workspace_bytes, unsigned flags, void *stream)
+{
+    const Outputs o{moments, s2_rows, s2_sums, psnr_rows, mse, noise_sums};
+    return run_frames(ref, dis, width, height, stride_bytes, bpc, nframes, features, o, workspace,
+                      workspace_bytes, static_cast<cudaStream_t>(stream), nullptr, flags);
 }
 
 int vmx_workspace_status(const void *workspace, void *stream)

@@ -94,6 +94,7 @@ struct Params {
     uint64_t *s2_sums, *noise_sums;
     uint32_t spin_limit;
     uint64_t launch;  // this launch's number (never 0): stamps finished items
+    uint32_t overlap; // launched to overlap the previous kernel on the stream
 };
 
 // Enqueue the frame kernel. `features` VMX_FEATURE_* bits; `vec` true when

@@ -1217,7 +1217,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
             end = c + k;
         }
         const int tk = (int)cur++;
-        if (tk >= nitems) break;
+        if (tk >= nitems) {
+            // Out of items: a kernel launched to overlap this one may start
+            // on the SMs that free up.
+            if (lane == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            break;
+        }
         int f, j;
         item_of_ticket(tk, p.frames, I, &f, &j);
         const int r0 = j * p.rows_per_item, r1 = min(H, r0 + p.rows_per_item);
@@ -1335,6 +1340,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         const int wf = wt / kParts, part = wt - wf * kParts;
         walk_part<TS, M, P, ODD, FULL, VEC>(p, wf, M ? part : 2);
     }
+    // Launched to overlap the previous kernel: finish after it, so that the
+    // stream's later work still follows both.
+    if (p.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC>
@@ -1358,8 +1366,23 @@ cudaError_t launch_one(const Params &p, const Layout &L, cudaStream_t stream)
     const long long warps = (long long)L.frames * L.items_per_frame;
     const long long blocks = (warps + kWarps - 1) / kWarps;
     const int grid = (int)std::min<long long>(blocks, (long long)sms * blocks_per_sm[dev]);
-    frames_kernel<TS, M, P, ODD, FULL, VEC><<<grid, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    if (!p.overlap) {
+        frames_kernel<TS, M, P, ODD, FULL, VEC><<<grid, kThreads, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
+    // Programmatic dependent launch: may start once every block of the
+    // previous kernel on the stream has run out of items or exited.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, frames_kernel<TS, M, P, ODD, FULL, VEC>, p);
 }
 
 template <typename TS, bool M, bool P, bool ODD, bool FULL>

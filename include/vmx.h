@@ -115,6 +115,35 @@ int vmx_moment_psnr_frames(const void *ref, const void *dis, int width, int heig
                            size_t workspace_bytes, void *stream);
 
 /*
+ * Pipelined batches. vmx_frames_ex() is vmx_moment_psnr_frames() with the
+ * features as bits (as in vmx_frames_host()) and `flags`:
+ *   VMX_FLAG_CLEARED  skip the call's clear of the workspace's control words:
+ *                     vmx_workspace_clear() did it on this stream since the
+ *                     workspace was last used.
+ *   VMX_FLAG_OVERLAP  launch the kernel so that it may start while the
+ *                     previous kernel on `stream` is finishing (programmatic
+ *                     dependent launch: on the SMs that kernel's blocks leave
+ *                     once they have run out of work). The caller guarantees
+ *                     that this call reads and writes nothing that kernel
+ *                     writes (another workspace, other outputs) and that the
+ *                     workspace was cleared beforehand (VMX_FLAG_CLEARED): a
+ *                     clear enqueued between the two kernels would separate
+ *                     them. The kernel does not finish before the previous
+ *                     one, so later work on the stream follows both.
+ * Both flags need a workspace. Errors as the other calls; unknown flags are
+ * VMX_EINVAL. The pages have no counterpart: this is how a stream of batches
+ * of one shape keeps the GPU busy between batches.
+ */
+#define VMX_FLAG_CLEARED 1u
+#define VMX_FLAG_OVERLAP 2u
+int vmx_workspace_clear(void *workspace, size_t workspace_bytes, int width, int height, int bpc,
+                        int nframes, int features, void *stream);
+int vmx_frames_ex(const void *ref, const void *dis, int width, int height, int64_t stride_bytes,
+                  int bpc, int nframes, int features, double *moments, uint64_t *s2_rows,
+                  uint64_t *s2_sums, uint64_t *psnr_rows, double *mse, uint64_t *noise_sums,
+                  void *workspace, size_t workspace_bytes, unsigned flags, void *stream);
+
+/*
  * Status of the last call that used `workspace`: VMX_OK, or VMX_ETIMEOUT if a
  * bounded device wait gave up. Synchronises `stream`.
  */

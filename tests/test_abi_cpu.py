@@ -120,3 +120,16 @@ def test_host_traffic(lib):
                                 ctypes.addressof(d2h))
     assert h2d.value == 2 * 16 * 2160 * 7680
     assert d2h.value == 16 * 4 * 8 + 16 * 2160 * 8 + 16 * 8
+
+
+def test_pipelining_flags_are_checked_before_any_cuda_call():
+    """Unknown flags, or flags without a workspace, are argument errors."""
+    lib = _lib.load()
+    p = ctypes.c_void_p(256)
+    assert lib.vmx_frames_ex(p, p, 64, 8, 128, 16, 1, 3, p, None, None, p, p, None, p, 1 << 20,
+                             4, None) == _lib.VMX_EINVAL
+    assert lib.vmx_frames_ex(p, p, 64, 8, 128, 16, 1, 3, p, None, None, p, p, None, None, 0,
+                             _lib.FLAG_CLEARED, None) == _lib.VMX_EINVAL
+    assert lib.vmx_workspace_clear(None, 1 << 20, 64, 8, 16, 1, 3, None) == _lib.VMX_EINVAL
+    assert lib.vmx_workspace_clear(p, 16, 64, 8, 16, 1, 3, None) == _lib.VMX_EINVAL
+

@@ -151,6 +151,28 @@ def test_graph_replays_match_calls():
         assert np.array_equal(u64(out["s2_sums"])[0], want["s2_sums"])
 
 
+def test_overlapped_batches_match_calls():
+    """Four batches per replay, each kernel launched to overlap the one
+    before: every batch's outputs equal a plain call's on its inputs."""
+    wl = synth.WORKLOADS["C4"]
+    ref, dis = wl.batch(4)
+    Rs = [to_device(ref[i:i + 1]) for i in range(4)]
+    Ds = [to_device(dis[i:i + 1]) for i in range(4)]
+    fg = api.FrameGraph(Rs[0], Ds[0], 16, s2_rows=True, sums=True, depth=4, refs=Rs, diss=Ds)
+    for _ in range(2):
+        fg.replay()
+        torch.cuda.synchronize()
+        assert fg.status() == 0
+        for i in range(4):
+            plain = api.frames(Rs[i], Ds[i], 16, s2_rows=True, sums=True)
+            torch.cuda.synchronize()
+            got = fg.outs[i]
+            for k in ("moments", "mse"):
+                assert same_doubles(got[k].cpu().numpy(), plain[k].cpu().numpy()), (i, k)
+            for k in ("psnr_rows", "s2_rows", "s2_sums", "noise_sums"):
+                assert np.array_equal(u64(got[k]), u64(plain[k])), (i, k)
+
+
 def test_launch_counter_counts_calls():
     wl = synth.WORKLOADS["C1"]
     ref, dis = wl.batch()
