@@ -53,6 +53,36 @@ def test_misaligned_past_2_53():
     run_and_check(ref, dis, 16, misalign=1)
 
 
+@pytest.mark.parametrize("bpc", [9, 11, 13, 14, 15])
+def test_other_depths(bpc):
+    """Scalers 2^1, 2^3, 2^5, 2^6, 2^7: ragged and packed rows, and a frame
+    above 2^21 pixels (the odd-counting instance)."""
+    ref, dis = _pair(100 + bpc, 2, 37, 1001, bpc, mode="extreme")
+    run_and_check(ref, dis, bpc)
+    rng = np.random.default_rng(200 + bpc)
+    top = 1 << bpc
+    ref = rng.integers(top // 2, top, size=(1, 1100, 2048), dtype=np.uint16)
+    dis = rng.integers(0, top, size=(1, 1100, 2048), dtype=np.uint16)
+    run_and_check(ref, dis, bpc)
+
+
+def test_misaligned_past_2_55():
+    """The scalar-load path through the look-back, the row runs from binade
+    55 up and the general walk (16-bit 4096x2560 near full scale)."""
+    wl = synth.WORKLOADS["T2"]
+    ref, dis = wl.batch()
+    run_and_check(ref, dis, 16, misalign=1)
+
+
+def test_ragged_width_past_2_53():
+    """A width that is not a multiple of 8 (a partial last vector) on a frame
+    past 2^53 units: the crossing row walk reads the row's tail by samples."""
+    rng = np.random.default_rng(12)
+    ref = rng.integers(40000, 65536, size=(2, 1440, 2563), dtype=np.uint16)
+    dis = rng.integers(40000, 65536, size=(2, 1440, 2563), dtype=np.uint16)
+    run_and_check(ref, dis, 16)
+
+
 def test_widest_rows_largest_frame():
     """32768-sample rows (2^15 terms, ADR-1499 "Decision" point 1) and a
     2^25-pixel frame past 2^53 units."""
