@@ -51,6 +51,24 @@ bool fail_at(const char *stage)
     return v && std::strcmp(v, stage) == 0;
 }
 
+// Tests of the bounded device waits: VMX_TEST_SPIN_LIMIT=n polls instead of
+// kSpinLimit, and VMX_TEST_WAIT_STALL=1 makes the walks wait for a block count
+// that is never reached, so that every such wait gives up and sets the
+// status word (the kernel still returns; nothing faults).
+uint32_t spin_limit_setting()
+{
+    const char *v = std::getenv("VMX_TEST_SPIN_LIMIT");
+    if (!v) return kSpinLimit;
+    const long n = std::strtol(v, nullptr, 10);
+    return n > 0 && n < (long)kSpinLimit ? (uint32_t)n : kSpinLimit;
+}
+
+bool wait_stall_setting()
+{
+    const char *v = std::getenv("VMX_TEST_WAIT_STALL");
+    return v && std::strcmp(v, "1") == 0;
+}
+
 int bytes_per_sample(int bpc) { return bpc == 8 ? 1 : 2; }
 
 }  // namespace
@@ -165,7 +183,8 @@ int run_frames(const void *ref, const void *dis, int width, int height, int64_t 
     p.mse = o.mse;
     p.s2_sums = o.s2_sums;
     p.noise_sums = o.noise_sums;
-    p.spin_limit = kSpinLimit;
+    p.spin_limit = spin_limit_setting();
+    p.test_stall = wait_stall_setting() ? 1u : 0u;
     p.launch = next_launch_number();
     p.overlap = (flags & VMX_FLAG_OVERLAP) ? 1u : 0u;
     const bool vec = (uintptr_t)ref % 16 == 0 && (uintptr_t)dis % 16 == 0 && stride % 16 == 0;

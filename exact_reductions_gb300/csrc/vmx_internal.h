@@ -95,6 +95,7 @@ struct Params {
     uint32_t spin_limit;
     uint64_t launch;  // this launch's number (never 0): stamps finished items
     uint32_t overlap; // launched to overlap the previous kernel on the stream
+    uint32_t test_stall;  // tests only: the walks wait for a count never reached
 };
 
 // Enqueue the frame kernel. `features` VMX_FEATURE_* bits; `vec` true when

@@ -733,7 +733,9 @@ __device__ __forceinline__ Agg agg_zero() { return Agg{{0, 0}, {0, 0}, 0, 0, 0, 
 // Items a block of frame blocks holds.
 __device__ __forceinline__ uint64_t block_items(const Params &p, int b)
 {
-    return (uint64_t)min(kBlockItems, p.items_per_frame - b * kBlockItems);
+    // (A test of the bounded waits asks for one item more than a block holds:
+    // a count nothing reaches.)
+    return (uint64_t)min(kBlockItems, p.items_per_frame - b * kBlockItems) + p.test_stall;
 }
 
 // Waits (bounded) until every block of frame f counts all its items, then
@@ -839,11 +841,10 @@ __device__ int crossing_item(const Params &p, int f, int X, SC *before)
         // Block `base` is incomplete: poll its items alone until the
         // crossing shows among its complete ones or all of them are out.
         const int i = base * kBlockItems + lane;
-        const int n = (int)block_items(p, base);
         for (;;) {
             bool di = true;
             SC vi{0, 0};
-            if (lane < n) {
+            if (i < I) {
                 di = ld_acquire64(&it[i].count) == p.launch;
                 if (di) vi = sums(it + i);
             }

@@ -203,6 +203,31 @@ def test_overlapped_batches_match_calls():
                 assert np.array_equal(u64(got[k]), u64(plain[k])), (i, k)
 
 
+def test_bounded_wait_gives_up_and_context_stays_usable(monkeypatch):
+    """A walk that waits for a block count nothing reaches gives up after the
+    poll limit, the call reports VMX_ETIMEOUT, and the next call is exact."""
+    from exact_reductions_gb300 import _lib
+    wl = synth.WORKLOADS["T1"]
+    ref, dis = wl.batch(1)
+    R, D = to_device(ref), to_device(dis)
+    monkeypatch.setenv("VMX_TEST_SPIN_LIMIT", "2000")
+    monkeypatch.setenv("VMX_TEST_WAIT_STALL", "1")
+    out = api.frames(R, D, 16)
+    torch.cuda.synchronize()
+    assert api.workspace_status(out["_workspace"]) == _lib.VMX_ETIMEOUT
+    # With no workspace the call waits for the result and returns the status.
+    with pytest.raises(_lib.VmxError) as err:
+        lib = _lib.load()
+        o = torch.empty((1, 4), dtype=torch.float64, device="cuda:0")
+        _lib.check(lib.vmx_moment_frames(R.data_ptr(), D.data_ptr(), wl.width, wl.height,
+                                         wl.width * 2, 16, 1, o.data_ptr(), None, None, None, 0,
+                                         torch.cuda.current_stream().cuda_stream), "stalled")
+    assert err.value.status == _lib.VMX_ETIMEOUT
+    monkeypatch.delenv("VMX_TEST_WAIT_STALL")
+    monkeypatch.delenv("VMX_TEST_SPIN_LIMIT")
+    run_and_check(ref, dis, 16)
+
+
 def test_launch_counter_counts_calls():
     wl = synth.WORKLOADS["C1"]
     ref, dis = wl.batch()
