@@ -64,6 +64,8 @@ def _bind(path: str) -> ctypes.CDLL:
     lib.vmx_oracle_moment_batch.restype = None
     lib.vmx_oracle_psnr_batch.argtypes = [vp, vp, i32, i32, i64, i32, i32, i32, u64p, dp]
     lib.vmx_oracle_psnr_batch.restype = None
+    lib.vmx_oracle_second_moment_lanes.argtypes = [vp, i32, i32, i64, i32, i32]
+    lib.vmx_oracle_second_moment_lanes.restype = ctypes.c_double
     lib.vmx_oracle_mutation.argtypes = []
     lib.vmx_oracle_mutation.restype = i32
     return lib
@@ -99,6 +101,17 @@ def moment(ref: np.ndarray, dis: np.ndarray, bpc: int, rows: bool = False,
                           out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                           r.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)) if rows else None)
     return (out, r) if rows else out
+
+
+def second_moment_lanes(plane: np.ndarray, bpc: int, lanes: int) -> float:
+    """Not the CPU's result: the second moment added in `lanes` interleaved
+    double accumulators, as a SIMD path that adds in lanes would (kept to
+    measure how far that is from the scalar sum past 2^53 units)."""
+    lib = load(0)
+    plane = np.ascontiguousarray(plane)
+    h, w = plane.shape
+    return float(lib.vmx_oracle_second_moment_lanes(plane.ctypes.data, w, h, plane.strides[0],
+                                                    bpc, lanes))
 
 
 def moment_sums(ref: np.ndarray, dis: np.ndarray, bpc: int, mutation: int = 0,

@@ -193,6 +193,35 @@ void vmx_oracle_moment(const void *ref, const void *dis, int width, int height,
     }
 }
 
+/* Not the CPU's result: the second moment as a SIMD path that adds in lanes
+ * forms it (the page on the exact second-moment sum, "Neutral / follow-ups":
+ * the NEON and SVE2 paths of the CPU extractor add in lanes, so past 2^53
+ * units they are not the scalar sum). Reading taken: `lanes` double
+ * accumulators, the pixel at raster position n going to lane n mod lanes,
+ * the lanes added left to right at the end. lanes == 1 is the scalar loop.
+ * Kept to measure that divergence; nothing in the library targets it. */
+double vmx_oracle_second_moment_lanes(const void *plane, int width, int height,
+                                      int64_t stride_bytes, int bpc, int lanes)
+{
+    double acc[16] = {0.0};
+    if (lanes < 1) lanes = 1;
+    if (lanes > 16) lanes = 16;
+    const float scaler = scaler_of(bpc);
+    long long n = 0;
+    for (int i = 0; i < height; ++i) {
+        const unsigned char *row = row_ptr(plane, stride_bytes, i);
+        for (int j = 0; j < width; ++j) {
+            float f = (float)sample_at(row, j, bpc) / scaler;
+            float sq = f * f;
+            acc[n % lanes] += (double)sq;
+            ++n;
+        }
+    }
+    double total = acc[0];
+    for (int l = 1; l < lanes; ++l) total += acc[l];
+    return total / pixel_count(width, height);
+}
+
 /* float_psnr.c::extract() as ADR-1499 "Context" states it: the binary32
  * square of each sample difference, a row's squares into a double
  * (noise_line()), the rows into one double in row order, then the CPU's
