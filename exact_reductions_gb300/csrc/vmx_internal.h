@@ -17,7 +17,7 @@ constexpr int kWarps = kThreads / 32;
 #define VMX_MIN_BLOCKS 3
 #endif
 #ifndef VMX_UNROLL
-#define VMX_UNROLL 4
+#define VMX_UNROLL 3
 #endif
 constexpr int kMinBlocks = VMX_MIN_BLOCKS; // CTAs per SM the kernel is compiled for
 constexpr int kMaxRowsPerItem = 32;        // rows per item, at most
@@ -26,7 +26,15 @@ constexpr int kMaxChunk = 4;               // items a warp takes per ticket, at 
 #define VMX_ITEM_PIXELS 4096
 #endif
 constexpr int kItemPixels = VMX_ITEM_PIXELS; // target pixels per warp item
+static_assert(kItemPixels <= 32768, "an item's odd-term counts must fit 16 bits");
 constexpr int kUnroll = VMX_UNROLL;        // 16-byte vectors in flight per lane per plane
+#ifndef VMX_FLUSH_SAMPLES
+#define VMX_FLUSH_SAMPLES 256
+#endif
+constexpr int kFlushSamples = VMX_FLUSH_SAMPLES; // 16-bit samples per lane and plane between flushes
+#ifndef VMX_WHOLE_LOADS
+#define VMX_WHOLE_LOADS 1
+#endif
 constexpr uint32_t kSpinLimit = 1u << 22;  // bounded look-back wait (polls)
 
 // Control words at the start of the workspace (cleared before each call).

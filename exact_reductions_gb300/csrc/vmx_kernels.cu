@@ -139,11 +139,17 @@ __device__ __forceinline__ uint4 load_vec(const unsigned char *row, int v, int w
 
 __device__ __forceinline__ int lane_id() { return (int)(threadIdx.x & 31); }
 
-__device__ __forceinline__ uint32_t warp_sum32(uint32_t v)
+// Warp total modulo 2^32 (one warp-wide reduction instruction).
+__device__ __forceinline__ uint32_t warp_sum32(uint32_t v) { return __reduce_add_sync(kFull, v); }
+
+// Warp total of values below 2^51 each (row and item sums): the low 24 bits
+// and the rest reduced apart as 32-bit sums, neither of which can wrap
+// (32 times 2^24, 32 times 2^27).
+__device__ __forceinline__ uint64_t warp_sum_lt51(uint64_t v)
 {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-    return v;
+    const uint32_t lo = warp_sum32((uint32_t)v & 0xFFFFFFu);
+    const uint32_t hi = warp_sum32((uint32_t)(v >> 24));
+    return ((uint64_t)hi << 24) + lo;
 }
 
 __device__ __forceinline__ uint64_t warp_sum(uint64_t v)
@@ -273,10 +279,11 @@ __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
     }
 }
 
-// Folds the sums since the last flush into the row sums. At most 64 samples
-// per lane and plane since the last flush keep every 32-bit sum below 2^30
-// (64 times 65535 times 255), every error sum below 2^13 and every odd-term
-// byte below 2^8.
+// Folds the sums since the last flush into the row sums. At most
+// kFlushSamples (256) samples per lane and plane since the last flush keep
+// every dot-product sum below 2^32 (256 times 65535 times 255), every error
+// sum below 2^15 (exact in binary32) and every odd-term byte below 2^8 (two
+// samples per word: 128 words add at most 128 to a byte).
 template <bool M, bool P, bool ODD>
 __device__ __forceinline__ void acc16_flush(Acc16 &a)
 {
@@ -306,26 +313,44 @@ __device__ __forceinline__ void acc16_flush(Acc16 &a)
 template <bool M, bool P, bool ODD, bool VEC>
 __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, int width)
 {
-    static_assert(kUnroll * 8 <= 64, "an iteration holds at most 64 samples per lane");
+    static_assert(kUnroll * 8 <= kFlushSamples, "an iteration holds at most kFlushSamples per lane");
+    static_assert(kFlushSamples <= 256, "dot-product sums must stay below 2^32");
     const int lane = lane_id();
     Acc16 a = {};
     const int nvt = (width + 7) >> 3;
+    // Vectors wholly inside the row (all of them but a ragged last one).
+    const int nfull = width >> 3;
     uint32_t pend = 0;  // samples per lane per plane since the last flush
     for (int base = 0; base < nvt; base += 32 * kUnroll) {
         // Vectors per lane this time (the same for the whole warp): kUnroll
         // but at the row's end, where vectors past it are skipped.
         const int nu = min(kUnroll, (nvt - base + 31) >> 5);
-        if (pend + 8 * nu > 64) {
+        if (pend + 8 * nu > kFlushSamples) {
             acc16_flush<M, P, ODD>(a);
             pend = 0;
         }
         uint4 R[kUnroll], D[kUnroll];
+#if VMX_WHOLE_LOADS
+        // Every vector of this iteration inside the row (the warp agrees):
+        // plain 16-byte loads without per-vector checks.
+        if (VEC && base + 32 * kUnroll <= nfull) {
+            const uint4 *vr = reinterpret_cast<const uint4 *>(rr) + base + lane;
+            const uint4 *vd = reinterpret_cast<const uint4 *>(dr) + base + lane;
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            if (u < nu) {
-                const int v = base + u * 32 + lane;
-                R[u] = load_vec<uint16_t, VEC>(rr, v, width);
-                D[u] = load_vec<uint16_t, VEC>(dr, v, width);
+            for (int u = 0; u < kUnroll; ++u) {
+                R[u] = ld_nc_v4(vr + 32 * u);
+                D[u] = ld_nc_v4(vd + 32 * u);
+            }
+        } else
+#endif
+        {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (u < nu) {
+                    const int v = base + u * 32 + lane;
+                    R[u] = load_vec<uint16_t, VEC>(rr, v, width);
+                    D[u] = load_vec<uint16_t, VEC>(dr, v, width);
+                }
             }
         }
 #pragma unroll
@@ -350,13 +375,12 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
     }
     if (P) out.tp = a.tp;
     // Row totals; the first-moment sums stay per lane (the item adds them).
-    out.t2r = warp_sum(out.t2r);
-    out.t2d = warp_sum(out.t2d);
-    out.tp = warp_sum(out.tp);
+    // (a lane's sums of a row stay below 2^42: at most 1024 terms below 2^32)
+    out.t2r = warp_sum_lt51(out.t2r);
+    out.t2d = warp_sum_lt51(out.t2d);
+    out.tp = warp_sum_lt51(out.tp);
     if (ODD) {  // both counts fit 16 bits (a row has at most 2^15 samples)
-        uint32_t packed = a.odd;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) packed += __shfl_xor_sync(kFull, packed, off);
+        const uint32_t packed = warp_sum32(a.odd);
         out.oddr = packed & 0xffffu;
         out.oddd = packed >> 16;
     }
@@ -395,9 +419,10 @@ __device__ RowSums row_sums8(const unsigned char *rr, const unsigned char *dr, i
         }
     }
     RowSums out;
-    out.t2r = warp_sum(s2r);
-    out.t2d = warp_sum(s2d);
-    out.tp = P ? out.t2r + out.t2d - 2ull * warp_sum(srd) : 0ull;
+    // A row's sums of 8-bit products stay below 2^31 (2^15 samples below 2^16).
+    out.t2r = warp_sum32(s2r);
+    out.t2d = warp_sum32(s2d);
+    out.tp = P ? out.t2r + out.t2d - 2ull * warp_sum32(srd) : 0ull;
     out.s1r = s1r;  // per lane; the item adds them
     out.s1d = s1d;
     out.oddr = out.oddd = 0;
@@ -1271,13 +1296,18 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         Agg g = agg_zero();
         const bool one = r1 - r0 == 1;
         if (M) {
-            g.s2[0] = one ? my_r : warp_sum(my_r);
-            g.s2[1] = one ? my_d : warp_sum(my_d);
+            g.s2[0] = one ? my_r : warp_sum_lt51(my_r);  // a row's sum is below 2^47
+            g.s2[1] = one ? my_d : warp_sum_lt51(my_d);
             g.s1[0] = warp_sum32(s1r);
             g.s1[1] = warp_sum32(s1d);
         }
-        if (ODD) g.odd = one ? my_o : warp_sum(my_o);
-        if (P) g.psnr = one ? my_p : warp_sum(my_p);
+        if (ODD && !one) {  // an item's counts fit 16 bits (at most 2^15 samples)
+            const uint32_t c = warp_sum32((uint32_t)my_o + ((uint32_t)(my_o >> 32) << 16));
+            g.odd = (uint64_t)(c & 0xffffu) | ((uint64_t)(c >> 16) << 32);
+        } else if (ODD) {
+            g.odd = my_o;
+        }
+        if (P) g.psnr = one ? my_p : warp_sum_lt51(my_p);
         if (lane == 0) {
             Agg *ia = p.items + (size_t)f * I + j;
             store_agg(ia, g);
