@@ -60,6 +60,16 @@ def lib_path() -> str:
     return _build.LIB
 
 
+def bind(path: str) -> ctypes.CDLL:
+    """Open a libvmx build at `path` with every entry point's signature set."""
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
 def load() -> ctypes.CDLL:
     """Load libvmx.so (built by ``exact_reductions_gb300.build.build_lib()``)."""
     global _lib
@@ -70,13 +80,8 @@ def load() -> ctypes.CDLL:
         raise ImportError(
             f"libvmx is not built ({path} missing): run "
             "`python -c 'import __graft_entry__ as g; g.build()'` first")
-    lib = ctypes.CDLL(path)
-    for name, (res, args) in SIGNATURES.items():
-        fn = getattr(lib, name)
-        fn.restype = res
-        fn.argtypes = args
-    _lib = lib
-    return lib
+    _lib = bind(path)
+    return _lib
 
 
 class VmxError(RuntimeError):

@@ -88,6 +88,30 @@ def build_lib(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, defines: List[str], force: bool = False) -> str:
+    """Compile libvmx with extra ``-D`` defines (compile-time alternatives of
+    the kernel, e.g. ``VMX_STAGES=3``) into ``_build/variants/<name>/``;
+    return the library's path."""
+    out = os.path.join(BUILD, "variants", name)
+    os.makedirs(out, exist_ok=True)
+    lib = os.path.join(out, "libvmx.so")
+    if not force and _newer(lib, _deps()):
+        return lib
+    flags = nvcc_flags([f"-D{d}" for d in defines])
+    objs, cmds = [], []
+    for src, lang in [(s, []) for s in CU_SOURCES] + [(s, ["-x", "cu"]) for s in CPP_SOURCES]:
+        obj = os.path.join(out, src + ".o")
+        objs.append(obj)
+        cmds.append([NVCC, *flags, *lang, "-c", os.path.join(CSRC, src), "-o", obj])
+    with ThreadPoolExecutor(max_workers=len(cmds)) as ex:
+        list(ex.map(_run, cmds))
+    tmp = lib + f".tmp{os.getpid()}"
+    _run([NVCC, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+          "-Xlinker", f"-rpath,{CUDA_HOME}/lib64"])
+    os.replace(tmp, lib)
+    return lib
+
+
 def build_model(force: bool = False) -> str:
     """Compile the CPU model of the ordered-sum steps (tests only)."""
     os.makedirs(BUILD, exist_ok=True)

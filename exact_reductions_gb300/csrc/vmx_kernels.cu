@@ -135,6 +135,126 @@ __device__ __forceinline__ uint4 load_vec(const unsigned char *row, int v, int w
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+__device__ __forceinline__ int lane_id_early() { return (int)(threadIdx.x & 31); }
+
+// ------------------------------------ bulk copies into shared memory ---
+//
+// A warp streams the whole 16-byte vectors of its item's rows through
+// kStages chunk buffers of its own in shared memory. A chunk is one pass of
+// the row loop: kUnroll x 32 vectors of each plane, copied by two bulk
+// asynchronous copies that lane 0 starts on the buffer's mbarrier; the warp
+// waits for the barrier's phase and reads the chunk with shared loads. A
+// buffer is refilled only after every lane has read it (a warp barrier, then
+// a proxy fence orders those reads before the copy's writes).
+
+constexpr int kChunkVecs = 32 * kUnroll;          // vectors per plane in a chunk
+constexpr uint32_t kChunkBytes = 16u * kChunkVecs;
+constexpr uint32_t kStageBytes = 2u * kChunkBytes;  // both planes
+constexpr size_t kPipeSmem = kStages > 0 ? (size_t)kWarps * kStages * (kStageBytes + 8u) : 0;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+
+// Bytes (a multiple of 16) from a 16-byte aligned global address to shared
+// memory, completing on `bar`.
+__device__ __forceinline__ void bulk_to_smem(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// A warp's chunk stream: chunks consumed (k) and started (n) over the warp's
+// life, which give each chunk its buffer (index mod kStages) and barrier
+// phase (index / kStages mod 2), and the next chunk of the current item to
+// start (row, chunk in the row).
+struct Pipe {
+    uint32_t buf, bar;  // shared addresses of the warp's buffers and barriers
+    uint32_t k, n;
+    int prow, pc;
+    bool broken;  // a wait gave up: later waits are skipped
+};
+
+// The rows [prow, r1) of one frame: chunks per row and plane bases.
+struct PipeSrc {
+    const unsigned char *fr, *fd;
+    int64_t stride;
+    int r1, cpr;
+};
+
+// Starts chunks until kStages are in flight or unread, or the item has no
+// more. Called by the whole warp (lane 0 issues) after a warp barrier.
+__device__ __forceinline__ void pipe_fill(Pipe &pp, const PipeSrc &src)
+{
+    while (src.cpr > 0 && pp.prow < src.r1 && pp.n < pp.k + (uint32_t)kStages) {
+        if (lane_id_early() == 0) {
+            const uint32_t st = pp.n % (uint32_t)kStages;
+            const uint32_t dst = pp.buf + st * kStageBytes, bar = pp.bar + 8u * st;
+            const int64_t off = (int64_t)pp.prow * src.stride + (int64_t)pp.pc * kChunkBytes;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_expect_tx(bar, kStageBytes);
+            bulk_to_smem(dst, src.fr + off, kChunkBytes, bar);
+            bulk_to_smem(dst + kChunkBytes, src.fd + off, kChunkBytes, bar);
+        }
+        ++pp.n;
+        if (++pp.pc == src.cpr) {
+            pp.pc = 0;
+            ++pp.prow;
+        }
+    }
+}
+
+// Waits (bounded) until chunk i is in shared memory.
+__device__ __forceinline__ void pipe_wait(Pipe &pp, uint32_t i, uint32_t *status)
+{
+    if (pp.broken) return;
+    const uint32_t bar = pp.bar + 8u * (i % (uint32_t)kStages), par = (i / (uint32_t)kStages) & 1u;
+    uint32_t spins = 0;
+    while (!mbar_try_wait(bar, par)) {
+        if (++spins > kPipeSpinLimit) {
+            if (lane_id_early() == 0) atomicOr(status, 1u);
+            pp.broken = true;
+            break;
+        }
+    }
+    pp.broken = __any_sync(0xffffffffu, pp.broken);
+}
+
 // ------------------------------------------------------- warp primitives ---
 
 __device__ __forceinline__ int lane_id() { return (int)(threadIdx.x & 31); }
@@ -310,8 +430,12 @@ __device__ __forceinline__ void acc16_flush(Acc16 &a)
     if (P) a.ep = make_float2(0.0f, 0.0f);
 }
 
-template <bool M, bool P, bool ODD, bool VEC>
-__device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, int width)
+// With STG the row's whole chunks come through the warp's chunk stream (the
+// row is the stream's next `cpr` chunks), the rest of the row straight from
+// global memory.
+template <bool M, bool P, bool ODD, bool VEC, bool STG>
+__device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, int width, Pipe &pp,
+                              const PipeSrc &src, uint32_t *status)
 {
     static_assert(kUnroll * 8 <= kFlushSamples, "an iteration holds at most kFlushSamples per lane");
     static_assert(kFlushSamples <= 256, "dot-product sums must stay below 2^32");
@@ -321,7 +445,32 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
     // Vectors wholly inside the row (all of them but a ragged last one).
     const int nfull = width >> 3;
     uint32_t pend = 0;  // samples per lane per plane since the last flush
-    for (int base = 0; base < nvt; base += 32 * kUnroll) {
+    int base = 0;
+    if (STG) {
+        const uint32_t lane_off = 16u * (uint32_t)lane;
+        for (int c = 0; c < src.cpr; ++c, base += kChunkVecs) {
+            if (pend + 8 * kUnroll > kFlushSamples) {
+                acc16_flush<M, P, ODD>(a);
+                pend = 0;
+            }
+            __syncwarp();  // every lane is done with the previous chunk's buffer
+            pipe_fill(pp, src);
+            pipe_wait(pp, pp.k, status);
+            const uint32_t at = pp.buf + (pp.k % (uint32_t)kStages) * kStageBytes + lane_off;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const uint4 R = lds128(at + 512u * u);
+                const uint4 D = lds128(at + kChunkBytes + 512u * u);
+                acc16_word<M, P, ODD>(a, R.x, D.x);
+                acc16_word<M, P, ODD>(a, R.y, D.y);
+                acc16_word<M, P, ODD>(a, R.z, D.z);
+                acc16_word<M, P, ODD>(a, R.w, D.w);
+            }
+            ++pp.k;
+            pend += 8 * kUnroll;
+        }
+    }
+    for (; base < nvt; base += 32 * kUnroll) {
         // Vectors per lane this time (the same for the whole warp): kUnroll
         // but at the row's end, where vectors past it are skipped.
         const int nu = min(kUnroll, (nvt - base + 31) >> 5);
@@ -1227,6 +1376,20 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
     // some warp's current item.
     __shared__ ulonglong4 item_rows[kWarps][kMaxRowsPerItem];  // sums of an item's rows
     const int wid = (int)(threadIdx.x >> 5);
+    // 16-bit rows on 16-byte boundaries stream through shared memory.
+    constexpr bool STG = kStages > 0 && VEC && sizeof(TS) == 2;
+    extern __shared__ __align__(128) unsigned char pipe_smem[];
+    Pipe pp{0u, 0u, 0u, 0u, 0, 0, false};
+    const int cpr = STG ? (p.width >> 3) / kChunkVecs : 0;  // whole chunks per row
+    if (STG) {
+        pp.buf = smem_u32(pipe_smem) + (uint32_t)wid * kStages * kStageBytes;
+        pp.bar = smem_u32(pipe_smem) + (uint32_t)kWarps * kStages * kStageBytes + 8u * kStages * (uint32_t)wid;
+        if (lane == 0) {
+            for (int st = 0; st < kStages; ++st) mbar_init(pp.bar + 8u * st);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncwarp();
+    }
     const uint32_t nwarps = gridDim.x * (uint32_t)kWarps;
     const uint32_t gwarp = blockIdx.x * (uint32_t)kWarps + (threadIdx.x >> 5);
     const uint32_t first = FULL ? 0u : nwarps;  // tickets below are assigned
@@ -1254,6 +1417,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         const int r0 = j * p.rows_per_item, r1 = min(H, r0 + p.rows_per_item);
         const unsigned char *fr = p.ref + (int64_t)f * p.pitch;
         const unsigned char *fd = p.dis + (int64_t)f * p.pitch;
+        const PipeSrc src{fr, fd, p.stride, r1, cpr};
+        if (STG) {  // start the item's first chunks
+            pp.prow = r0;
+            pp.pc = 0;
+            __syncwarp();
+            pipe_fill(pp, src);
+        }
 
         // A. exact row sums. Lane 0 records each row and keeps its sums in
         // the warp's shared slots, so that no item totals stay live in
@@ -1262,8 +1432,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         for (int r = r0; r < r1; ++r) {
             const unsigned char *rr = fr + (int64_t)r * p.stride;
             const unsigned char *dr = fd + (int64_t)r * p.stride;
-            const RowSums rs = sizeof(TS) == 2 ? row_sums16<M, P, ODD, VEC>(rr, dr, p.width)
-                                               : row_sums8<M, P, VEC>(rr, dr, p.width);
+            const RowSums rs = sizeof(TS) == 2
+                                   ? row_sums16<M, P, ODD, VEC, STG>(rr, dr, p.width, pp, src, p.status)
+                                   : row_sums8<M, P, VEC>(rr, dr, p.width);
             if (lane == 0) {
                 if (M) {
                     p.s2_rows[((size_t)f * 2) * H + r] = rs.t2r;
@@ -1358,6 +1529,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         }
     }
 
+    // Every chunk a warp started it has read, unless a wait gave up: then
+    // wait (bounded) for the copies still landing in its buffers.
+    if (STG && pp.broken) {
+        pp.broken = false;
+        for (uint32_t i = pp.n > (uint32_t)kStages ? pp.n - kStages : 0u; i < pp.n; ++i) pipe_wait(pp, i, p.status);
+    }
+
     // D. Walks. A warp out of items takes a part of a frame to walk (the ref
     // moments, the dis moments, the psnr noise). Its waits on the frame's
     // blocks are bounded; the items they wait for are held by warps that are
@@ -1384,10 +1562,17 @@ cudaError_t launch_one(const Params &p, const Layout &L, cudaStream_t stream)
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    // Chunk buffers of the 16-bit kernels that stream through shared memory.
+    const size_t smem = kStages > 0 && VEC && sizeof(TS) == 2 ? kPipeSmem : 0;
     if (blocks_per_sm[dev] == 0) {
+        if (smem > 0) {
+            err = cudaFuncSetAttribute(frames_kernel<TS, M, P, ODD, FULL, VEC>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (err != cudaSuccess) return err;
+        }
         int n = 0;
         err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, frames_kernel<TS, M, P, ODD, FULL, VEC>, kThreads, 0);
+            &n, frames_kernel<TS, M, P, ODD, FULL, VEC>, kThreads, smem);
         if (err != cudaSuccess) return err;
         blocks_per_sm[dev] = n > 0 ? n : 1;
     }
@@ -1398,7 +1583,7 @@ cudaError_t launch_one(const Params &p, const Layout &L, cudaStream_t stream)
     const long long blocks = (warps + kWarps - 1) / kWarps;
     const int grid = (int)std::min<long long>(blocks, (long long)sms * blocks_per_sm[dev]);
     if (!p.overlap) {
-        frames_kernel<TS, M, P, ODD, FULL, VEC><<<grid, kThreads, 0, stream>>>(p);
+        frames_kernel<TS, M, P, ODD, FULL, VEC><<<grid, kThreads, smem, stream>>>(p);
         return cudaGetLastError();
     }
     // Programmatic dependent launch: may start once every block of the
@@ -1406,7 +1591,7 @@ cudaError_t launch_one(const Params &p, const Layout &L, cudaStream_t stream)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
