@@ -148,6 +148,7 @@ __device__ __forceinline__ int lane_id_early() { return (int)(threadIdx.x & 31);
 // a proxy fence orders those reads before the copy's writes).
 
 constexpr int kChunkVecs = 32 * kUnroll;          // vectors per plane in a chunk
+constexpr uint32_t kNStages = kStages > 0 ? (uint32_t)kStages : 1u;  // buffers (at least one, for the modulo)
 constexpr uint32_t kChunkBytes = 16u * kChunkVecs;
 constexpr uint32_t kStageBytes = 2u * kChunkBytes;  // both planes
 constexpr size_t kPipeSmem = kStages > 0 ? (size_t)kWarps * kStages * (kStageBytes + 8u) : 0;
@@ -223,7 +224,7 @@ __device__ __forceinline__ void pipe_fill(Pipe &pp, const PipeSrc &src)
 {
     while (src.cpr > 0 && pp.prow < src.r1 && pp.n < pp.k + (uint32_t)kStages) {
         if (lane_id_early() == 0) {
-            const uint32_t st = pp.n % (uint32_t)kStages;
+            const uint32_t st = pp.n % kNStages;
             const uint32_t dst = pp.buf + st * kStageBytes, bar = pp.bar + 8u * st;
             const int64_t off = (int64_t)pp.prow * src.stride + (int64_t)pp.pc * kChunkBytes;
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -243,7 +244,7 @@ __device__ __forceinline__ void pipe_fill(Pipe &pp, const PipeSrc &src)
 __device__ __forceinline__ void pipe_wait(Pipe &pp, uint32_t i, uint32_t *status)
 {
     if (pp.broken) return;
-    const uint32_t bar = pp.bar + 8u * (i % (uint32_t)kStages), par = (i / (uint32_t)kStages) & 1u;
+    const uint32_t bar = pp.bar + 8u * (i % kNStages), par = (i / kNStages) & 1u;
     uint32_t spins = 0;
     while (!mbar_try_wait(bar, par)) {
         if (++spins > kPipeSpinLimit) {
@@ -344,21 +345,25 @@ struct RowSums {
 // with f = p exact in binary32 (g = 2^23 + p as bits, less 2^23); the errors
 // are integers of at most 2^7 and add exactly in binary32.
 // Odd terms: a binary32 square of a codeword is odd exactly when the codeword
-// is odd and below 4096, i.e. its low byte is odd and its high byte below 16;
-// four samples (two per plane) are tested at once in byte lanes.
+// is odd and below 4096, i.e. its bits 0 and 12-15 read 1 and 0; the even
+// terms are counted (two samples a word, in halfword lanes) and the row's
+// end takes them from its number of samples.
 // First moments: integer sums of g over the row, the 2^23 bias taken off at
 // the row's end (the true sums fit 32 bits, so the wrap-around is harmless).
 // Each flush folds its rounding errors into the row's term sums at once.
 struct Acc16 {
     uint32_t lr, hr, ld, hd, lx, hx;  // dot-product sums since the last flush
-    uint32_t oddb;                    // odd terms since the last flush, one byte per sample slot
+    uint32_t nzr, nzd;                // samples with even terms since the last flush, per halfword
     float2 er, ed, ep;                // rounding errors since the last flush
     uint32_t gsr, gsd;                // row sums of g
-    uint32_t odd;                     // row's odd terms (ref low half, dis high)
+    uint32_t even;                    // row's even terms (ref low half, dis high)
     uint64_t t2r, t2d, tp;            // row sums of the terms: squares of p, of q, of d
 };
 
 __device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
+
+// Each unsigned halfword of x, or 1 if that is smaller.
+__device__ __forceinline__ uint32_t halfword_min1(uint32_t x) { return __vminu2(x, 0x00010001u); }
 
 template <bool M, bool P, bool ODD>
 __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
@@ -383,9 +388,11 @@ __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
         a.er = __fadd2_rn(a.er, __ffma2_rn(fr, fr, neg2(__fmul2_rn(fr, fr))));
         a.ed = __fadd2_rn(a.ed, __ffma2_rn(fd, fd, neg2(__fmul2_rn(fd, fd))));
         if (ODD) {
-            const uint32_t lo = __byte_perm(r, d, 0x6420), hi = __byte_perm(r, d, 0x7531);
-            const uint32_t big = ((hi & 0x7F7F7F7Fu) + 0x70707070u) | hi;  // bit 7: byte >= 16
-            a.oddb += lo & ~(big >> 7) & 0x01010101u;
+            // Per 16-bit sample: zero exactly when it is odd and below 4096;
+            // the unsigned halfword minimum with 1 counts the others.
+            const uint32_t tr = (r & 0xF001F001u) ^ 0x00010001u, td = (d & 0xF001F001u) ^ 0x00010001u;
+            a.nzr += halfword_min1(tr);
+            a.nzd += halfword_min1(td);
         }
     }
     if (P) {
@@ -402,8 +409,8 @@ __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
 // Folds the sums since the last flush into the row sums. At most
 // kFlushSamples (256) samples per lane and plane since the last flush keep
 // every dot-product sum below 2^32 (256 times 65535 times 255), every error
-// sum below 2^15 (exact in binary32) and every odd-term byte below 2^8 (two
-// samples per word: 128 words add at most 128 to a byte).
+// sum below 2^15 (exact in binary32) and every even-term halfword count at
+// most 128 (two samples a word: 128 words add at most 128 to a halfword).
 template <bool M, bool P, bool ODD>
 __device__ __forceinline__ void acc16_flush(Acc16 &a)
 {
@@ -421,8 +428,8 @@ __device__ __forceinline__ void acc16_flush(Acc16 &a)
         a.lr = a.hr = a.ld = a.hd = 0;
         a.er = a.ed = make_float2(0.0f, 0.0f);
         if (ODD) {
-            a.odd += (a.oddb & 0x00FF00FFu) + ((a.oddb >> 8) & 0x00FF00FFu);
-            a.oddb = 0;
+            a.even += ((a.nzr & 0xffffu) + (a.nzr >> 16)) | (((a.nzd & 0xffffu) + (a.nzd >> 16)) << 16);
+            a.nzr = a.nzd = 0;
         }
     } else if (P) {
         a.tp -= (uint64_t)ep;
@@ -456,7 +463,7 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
             __syncwarp();  // every lane is done with the previous chunk's buffer
             pipe_fill(pp, src);
             pipe_wait(pp, pp.k, status);
-            const uint32_t at = pp.buf + (pp.k % (uint32_t)kStages) * kStageBytes + lane_off;
+            const uint32_t at = pp.buf + (pp.k % kNStages) * kStageBytes + lane_off;
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const uint4 R = lds128(at + 512u * u);
@@ -529,7 +536,8 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
     out.t2d = warp_sum_lt51(out.t2d);
     out.tp = warp_sum_lt51(out.tp);
     if (ODD) {  // both counts fit 16 bits (a row has at most 2^15 samples)
-        const uint32_t packed = warp_sum32(a.odd);
+        const uint32_t nl = 8u * (uint32_t)((nvt + 31) >> 5);  // samples per lane and plane
+        const uint32_t packed = warp_sum32((nl | (nl << 16)) - a.even);
         out.oddr = packed & 0xffffu;
         out.oddd = packed >> 16;
     }
