@@ -41,6 +41,9 @@ constexpr int kFlushSamples = VMX_FLUSH_SAMPLES; // 16-bit samples per lane and 
 // 16-bit 3840x2160 batch takes about 9% longer).
 constexpr int kStages = VMX_STAGES;
 constexpr uint32_t kPipeSpinLimit = 1u << 20;  // polls of one chunk's barrier, at most
+#ifndef VMX_G_DP2A
+#define VMX_G_DP2A 0
+#endif
 #ifndef VMX_WHOLE_LOADS
 #define VMX_WHOLE_LOADS 1
 #endif

@@ -346,16 +346,15 @@ struct RowSums {
 // are integers of at most 2^7 and add exactly in binary32.
 // Odd terms: a binary32 square of a codeword is odd exactly when the codeword
 // is odd and below 4096, i.e. its bits 0 and 12-15 read 1 and 0; the even
-// terms are counted (two samples a word, in halfword lanes) and the row's
-// end takes them from its number of samples.
-// First moments: integer sums of g over the row, the 2^23 bias taken off at
-// the row's end (the true sums fit 32 bits, so the wrap-around is harmless).
+// terms are counted (a halfword minimum marks them, a dot product adds the
+// marks) and the row's end takes them from its number of samples.
+// First moments: the samples' sums by a dot product with (1, 1).
 // Each flush folds its rounding errors into the row's term sums at once.
 struct Acc16 {
     uint32_t lr, hr, ld, hd, lx, hx;  // dot-product sums since the last flush
-    uint32_t nzr, nzd;                // samples with even terms since the last flush, per halfword
+    uint32_t nzr, nzd;                // samples with even terms since the last flush
     float2 er, ed, ep;                // rounding errors since the last flush
-    uint32_t gsr, gsd;                // row sums of g
+    uint32_t s1r, s1d;                // row sums of the samples (first moments)
     uint32_t even;                    // row's even terms (ref low half, dis high)
     uint64_t t2r, t2d, tp;            // row sums of the terms: squares of p, of q, of d
 };
@@ -368,8 +367,13 @@ __device__ __forceinline__ uint32_t halfword_min1(uint32_t x) { return __vminu2(
 template <bool M, bool P, bool ODD>
 __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
 {
+#if VMX_G_DP2A
+    const uint32_t gr0 = __dp2a_lo(r, 0x00000001u, kA), gr1 = __dp2a_lo(r, 0x00000100u, kA);
+    const uint32_t gd0 = __dp2a_lo(d, 0x00000001u, kA), gd1 = __dp2a_lo(d, 0x00000100u, kA);
+#else
     const uint32_t gr0 = __byte_perm(r, kA, 0x7610), gr1 = __byte_perm(r, kA, 0x7632);
     const uint32_t gd0 = __byte_perm(d, kA, 0x7610), gd1 = __byte_perm(d, kA, 0x7632);
+#endif
     const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
     const float2 fr = __fadd2_rn(make_float2(__uint_as_float(gr0), __uint_as_float(gr1)), m23);
     const float2 fd = __fadd2_rn(make_float2(__uint_as_float(gd0), __uint_as_float(gd1)), m23);
@@ -383,16 +387,16 @@ __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
             a.lx = __dp2a_lo(r, xd, a.lx);
             a.hx = __dp2a_hi(r, xd, a.hx);
         }
-        a.gsr += gr0 + gr1;
-        a.gsd += gd0 + gd1;
+        a.s1r = __dp2a_lo(r, 0x00000101u, a.s1r);  // p0 + p1
+        a.s1d = __dp2a_lo(d, 0x00000101u, a.s1d);
         a.er = __fadd2_rn(a.er, __ffma2_rn(fr, fr, neg2(__fmul2_rn(fr, fr))));
         a.ed = __fadd2_rn(a.ed, __ffma2_rn(fd, fd, neg2(__fmul2_rn(fd, fd))));
         if (ODD) {
             // Per 16-bit sample: zero exactly when it is odd and below 4096;
             // the unsigned halfword minimum with 1 counts the others.
             const uint32_t tr = (r & 0xF001F001u) ^ 0x00010001u, td = (d & 0xF001F001u) ^ 0x00010001u;
-            a.nzr += halfword_min1(tr);
-            a.nzd += halfword_min1(td);
+            a.nzr = __dp2a_lo(halfword_min1(tr), 0x00000101u, a.nzr);
+            a.nzd = __dp2a_lo(halfword_min1(td), 0x00000101u, a.nzd);
         }
     }
     if (P) {
@@ -409,8 +413,7 @@ __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
 // Folds the sums since the last flush into the row sums. At most
 // kFlushSamples (256) samples per lane and plane since the last flush keep
 // every dot-product sum below 2^32 (256 times 65535 times 255), every error
-// sum below 2^15 (exact in binary32) and every even-term halfword count at
-// most 128 (two samples a word: 128 words add at most 128 to a halfword).
+// sum below 2^15 (exact in binary32) and every even-term count at most 256.
 template <bool M, bool P, bool ODD>
 __device__ __forceinline__ void acc16_flush(Acc16 &a)
 {
@@ -428,7 +431,7 @@ __device__ __forceinline__ void acc16_flush(Acc16 &a)
         a.lr = a.hr = a.ld = a.hd = 0;
         a.er = a.ed = make_float2(0.0f, 0.0f);
         if (ODD) {
-            a.even += ((a.nzr & 0xffffu) + (a.nzr >> 16)) | (((a.nzd & 0xffffu) + (a.nzd >> 16)) << 16);
+            a.even += a.nzr | (a.nzd << 16);
             a.nzr = a.nzd = 0;
         }
     } else if (P) {
@@ -523,11 +526,10 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
     acc16_flush<M, P, ODD>(a);
     RowSums out = {0, 0, 0, 0, 0, 0, 0};
     if (M) {
-        const uint32_t n = 8u * (uint32_t)((nvt + 31) >> 5);  // samples per lane, zeros included
         out.t2r = a.t2r;
         out.t2d = a.t2d;
-        out.s1r = a.gsr - n * kA;
-        out.s1d = a.gsd - n * kA;
+        out.s1r = a.s1r;
+        out.s1d = a.s1d;
     }
     if (P) out.tp = a.tp;
     // Row totals; the first-moment sums stay per lane (the item adds them).
