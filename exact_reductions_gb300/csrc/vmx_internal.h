@@ -21,7 +21,10 @@ constexpr int kWarps = kThreads / 32;
 #endif
 constexpr int kMinBlocks = VMX_MIN_BLOCKS; // CTAs per SM the kernel is compiled for
 constexpr int kMaxRowsPerItem = 32;        // rows per item, at most
-constexpr int kMaxChunk = 4;               // items a warp takes per ticket, at most
+#ifndef VMX_MAX_CHUNK
+#define VMX_MAX_CHUNK 4
+#endif
+constexpr int kMaxChunk = VMX_MAX_CHUNK;   // items a warp takes per ticket, at most
 #ifndef VMX_ITEM_PIXELS
 #define VMX_ITEM_PIXELS 4096
 #endif
