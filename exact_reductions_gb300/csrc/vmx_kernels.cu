@@ -590,47 +590,86 @@ __device__ RowSums row_sums8(const unsigned char *rr, const unsigned char *dr, i
 
 // ------------------------------------------------ phase B: row runs ---
 
-// The run of a 16-bit row under binade e: segments of 32 lanes x 8 samples,
-// each lane's 8 terms a compact run, lanes composed by an order-preserving
-// shuffle tree (lane i takes lane i + off), segments composed in order.
+// 16-byte vector v of a 16-bit row through L1 (zero past the row's end):
+// the run pass reads each lane's vectors three apart, so neighbouring loads
+// share cache lines.
+template <bool VEC>
+__device__ __forceinline__ uint4 load_vec16_l1(const unsigned char *row, int v, int width)
+{
+    const int j0 = v << 3;
+    if (VEC && j0 + 8 <= width) return __ldg(reinterpret_cast<const uint4 *>(row) + v);
+    return load_vec<uint16_t, VEC>(row, v, width);
+}
+
+// The compact run of n consecutive terms under last place u = 2^sh (the
+// method of lane_run_fp in ordsum.cuh, with both start parities' binary32
+// trajectories advanced by one packed add). Valid while n * 2u < 2^22 (the
+// trajectory offsets stay exact small integers): n = 24 up to sh = 16.
+template <int N>
+__device__ __forceinline__ LaneRun lane_run_fp2(const uint32_t (&t)[N], int sh)
+{
+    const float uf = __uint_as_float((uint32_t)(127 + sh) << 23);  // 2^sh
+    const float f0e = __fmul_rn(12582912.0f, uf);                // 1.5 * 2^23 * u
+    const float2 f0 = make_float2(f0e, __fadd_rn(f0e, uf));
+    float2 F = f0;
+    uint32_t tlo = 0, vsum = 0;
+    const uint32_t vmask = (2u << sh) - 1u;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const uint32_t v = t[i] & vmask;
+        tlo += t[i];
+        vsum += v;
+        const float vf = __fadd_rn(__uint_as_float(v | 0x4B000000u), -8388608.0f);
+        F = __fadd2_rn(F, make_float2(vf, vf));
+    }
+    const float2 dF = __fadd2_rn(F, make_float2(-f0.x, -f0.y));
+    LaneRun r;
+    r.tlo = tlo;
+    r.d[0] = (int32_t)(__float_as_uint(__fadd_rn(dF.x, 12582912.0f)) - 0x4B400000u) - (int32_t)vsum;
+    r.d[1] = (int32_t)(__float_as_uint(__fadd_rn(dF.y, 12582912.0f)) - 0x4B400000u) - (int32_t)vsum;
+    return r;
+}
+
+// The run of a 16-bit row under binade e: passes of 32 lanes x 24 samples,
+// each lane's 24 consecutive terms a compact run, lanes composed by an
+// order-preserving shuffle tree (lane i takes lane i + off), passes composed
+// in order. Samples past the row are zero terms, which leave any run as it is.
 template <bool VEC>
 __device__ __noinline__ Run row_run16(const unsigned char *row, int width, int e, uint64_t exact)
 {
+    constexpr int kRunVecs = 3;  // consecutive vectors per lane and pass
     const int lane = lane_id();
     const int sh = e - 52;
     const int nvt = (width + 7) >> 3;
     LaneRun acc = lane_identity();
-    for (int base = 0; base < nvt; base += 32 * kUnroll) {
-        uint4 V[kUnroll];
+    for (int base = 0; base < nvt; base += 32 * kRunVecs) {
+        uint32_t t[8 * kRunVecs];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) V[u] = load_vec<uint16_t, VEC>(row, base + u * 32 + lane, width);
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            if (base + u * 32 >= nvt) break;  // warp-uniform
-            const uint32_t w4[4] = {V[u].x, V[u].y, V[u].z, V[u].w};
-            uint32_t t[8];
+        for (int u = 0; u < kRunVecs; ++u) {
+            const uint4 V = load_vec16_l1<VEC>(row, base + lane * kRunVecs + u, width);
+            const uint32_t w4[4] = {V.x, V.y, V.z, V.w};
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 const uint32_t g0 = __byte_perm(w4[w], kA, 0x7610);
                 const uint32_t g1 = __byte_perm(w4[w], kA, 0x7632);
-                t[2 * w] = term_from_float(w4[w] & 0xffffu, __fsub_rn(__uint_as_float(g0), 8388608.0f));
-                t[2 * w + 1] = term_from_float(w4[w] >> 16, __fsub_rn(__uint_as_float(g1), 8388608.0f));
+                t[8 * u + 2 * w] = term_from_float(w4[w] & 0xffffu, __fsub_rn(__uint_as_float(g0), 8388608.0f));
+                t[8 * u + 2 * w + 1] = term_from_float(w4[w] >> 16, __fsub_rn(__uint_as_float(g1), 8388608.0f));
             }
-            LaneRun l = lane_run_fp(t, 8, sh);
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                LaneRun o;
-                o.tlo = __shfl_down_sync(kFull, l.tlo, off);
-                o.d[0] = __shfl_down_sync(kFull, l.d[0], off);
-                o.d[1] = __shfl_down_sync(kFull, l.d[1], off);
-                if ((lane & (2 * off - 1)) == 0) l = lane_compose(l, o, sh);
-            }
-            LaneRun seg;
-            seg.tlo = __shfl_sync(kFull, l.tlo, 0);
-            seg.d[0] = __shfl_sync(kFull, l.d[0], 0);
-            seg.d[1] = __shfl_sync(kFull, l.d[1], 0);
-            acc = lane_compose(acc, seg, sh);
         }
+        LaneRun l = lane_run_fp2(t, sh);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            LaneRun o;
+            o.tlo = __shfl_down_sync(kFull, l.tlo, off);
+            o.d[0] = __shfl_down_sync(kFull, l.d[0], off);
+            o.d[1] = __shfl_down_sync(kFull, l.d[1], off);
+            if ((lane & (2 * off - 1)) == 0) l = lane_compose(l, o, sh);
+        }
+        LaneRun seg;
+        seg.tlo = __shfl_sync(kFull, l.tlo, 0);
+        seg.d[0] = __shfl_sync(kFull, l.d[0], 0);
+        seg.d[1] = __shfl_sync(kFull, l.d[1], 0);
+        acc = lane_compose(acc, seg, sh);
     }
     return lane_to_run(acc, exact);
 }
