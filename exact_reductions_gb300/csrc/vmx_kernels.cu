@@ -601,6 +601,20 @@ __device__ __forceinline__ uint4 load_vec16_l1(const unsigned char *row, int v, 
     return load_vec<uint16_t, VEC>(row, v, width);
 }
 
+// The binary32 squares of a word's two 16-bit samples as the exact
+// integers they are (term_from_float in ordsum.cuh, two samples at a time):
+// p^2 less the product's rounding error, which a fused multiply-add gives.
+__device__ __forceinline__ void terms_of_word(uint32_t w, uint32_t *t0, uint32_t *t1)
+{
+    const uint32_t p0 = w & 0xffffu, p1 = w >> 16;
+    const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
+    const float2 f = __fadd2_rn(make_float2(__uint_as_float(p0 | kA), __uint_as_float(p1 | kA)), m23);
+    const float2 e = __ffma2_rn(f, f, neg2(__fmul2_rn(f, f)));  // integers in [-128, 128]
+    const float2 ei = __fadd2_rn(e, make_float2(12582912.0f, 12582912.0f));
+    *t0 = p0 * p0 - (__float_as_uint(ei.x) - 0x4B400000u);
+    *t1 = p1 * p1 - (__float_as_uint(ei.y) - 0x4B400000u);
+}
+
 // The compact run of n consecutive terms under last place u = 2^sh (the
 // method of lane_run_fp in ordsum.cuh, with both start parities' binary32
 // trajectories advanced by one packed add). Valid while n * 2u < 2^22 (the
@@ -608,19 +622,22 @@ __device__ __forceinline__ uint4 load_vec16_l1(const unsigned char *row, int v, 
 template <int N>
 __device__ __forceinline__ LaneRun lane_run_fp2(const uint32_t (&t)[N], int sh)
 {
+    static_assert(N % 2 == 0, "terms come in pairs");
     const float uf = __uint_as_float((uint32_t)(127 + sh) << 23);  // 2^sh
     const float f0e = __fmul_rn(12582912.0f, uf);                // 1.5 * 2^23 * u
     const float2 f0 = make_float2(f0e, __fadd_rn(f0e, uf));
     float2 F = f0;
     uint32_t tlo = 0, vsum = 0;
     const uint32_t vmask = (2u << sh) - 1u;
+    const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const uint32_t v = t[i] & vmask;
-        tlo += t[i];
-        vsum += v;
-        const float vf = __fadd_rn(__uint_as_float(v | 0x4B000000u), -8388608.0f);
-        F = __fadd2_rn(F, make_float2(vf, vf));
+    for (int i = 0; i < N; i += 2) {
+        const uint32_t v0 = t[i] & vmask, v1 = t[i + 1] & vmask;
+        tlo += t[i] + t[i + 1];
+        vsum += v0 + v1;
+        const float2 vf = __fadd2_rn(make_float2(__uint_as_float(v0 | kA), __uint_as_float(v1 | kA)), m23);
+        F = __fadd2_rn(F, make_float2(vf.x, vf.x));
+        F = __fadd2_rn(F, make_float2(vf.y, vf.y));
     }
     const float2 dF = __fadd2_rn(F, make_float2(-f0.x, -f0.y));
     LaneRun r;
@@ -649,12 +666,7 @@ __device__ __noinline__ Run row_run16(const unsigned char *row, int width, int e
             const uint4 V = load_vec16_l1<VEC>(row, base + lane * kRunVecs + u, width);
             const uint32_t w4[4] = {V.x, V.y, V.z, V.w};
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const uint32_t g0 = __byte_perm(w4[w], kA, 0x7610);
-                const uint32_t g1 = __byte_perm(w4[w], kA, 0x7632);
-                t[8 * u + 2 * w] = term_from_float(w4[w] & 0xffffu, __fsub_rn(__uint_as_float(g0), 8388608.0f));
-                t[8 * u + 2 * w + 1] = term_from_float(w4[w] >> 16, __fsub_rn(__uint_as_float(g1), 8388608.0f));
-            }
+            for (int w = 0; w < 4; ++w) terms_of_word(w4[w], &t[8 * u + 2 * w], &t[8 * u + 2 * w + 1]);
         }
         LaneRun l = lane_run_fp2(t, sh);
 #pragma unroll
