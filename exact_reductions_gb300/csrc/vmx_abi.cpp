@@ -79,13 +79,18 @@ bool make_layout(int width, int height, int bpc, int frames, int features, Layou
         return false;
     if ((int64_t)width * height > (int64_t)1 << 25) return false;
     if (features < 1 || features > 3) return false;
-    const int rpi = std::min(kMaxRowsPerItem, std::max(1, (kItemPixels + width - 1) / width));
+    const int64_t n = (int64_t)width * height;
+    const bool m = features & VMX_FEATURE_MOMENT;
+    // Terms are below 2^32 units: a frame of n pixels stays at or below 2^53
+    // units when n <= 2^21 and below 2^55 when n <= 2^23.
+    L->ordered = m && bpc > 8 && n > ((int64_t)1 << 21);
+    L->full = L->ordered && n > ((int64_t)1 << 23);
+    const int target = L->full ? kItemPixelsFull : kItemPixels;
+    const int rpi = std::min(kMaxRowsPerItem, std::max(1, (target + width - 1) / width));
     const int ipf = (height + rpi - 1) / rpi;
     const int bpf = (ipf + kBlockItems - 1) / kBlockItems;
     if ((int64_t)frames * ipf >= (int64_t)INT_MAX / 2) return false;
     const size_t F = (size_t)frames, I = (size_t)ipf, B = (size_t)bpf, H = (size_t)height;
-    const int64_t n = (int64_t)width * height;
-    const bool m = features & VMX_FEATURE_MOMENT;
     L->width = width;
     L->height = height;
     L->frames = frames;
@@ -94,10 +99,6 @@ bool make_layout(int width, int height, int bpc, int frames, int features, Layou
     L->rows_per_item = rpi;
     L->items_per_frame = ipf;
     L->blocks_per_frame = bpf;
-    // Terms are below 2^32 units: a frame of n pixels stays at or below 2^53
-    // units when n <= 2^21 and below 2^55 when n <= 2^23.
-    L->ordered = m && bpc > 8 && n > ((int64_t)1 << 21);
-    L->full = L->ordered && n > ((int64_t)1 << 23);
     size_t off = 0;
     L->off_ctrl = off;
     off = align256(off + (kCtrlWords + (L->full ? F * I : 0)) * sizeof(uint32_t));

@@ -29,7 +29,13 @@ constexpr int kMaxChunk = VMX_MAX_CHUNK;   // items a warp takes per ticket, at 
 #define VMX_ITEM_PIXELS 4096
 #endif
 constexpr int kItemPixels = VMX_ITEM_PIXELS; // target pixels per warp item
-static_assert(kItemPixels <= 32768, "an item's odd-term counts must fit 16 bits");
+#ifndef VMX_ITEM_PIXELS_FULL
+#define VMX_ITEM_PIXELS_FULL 32768
+#endif
+// Target pixels per item where the look-back runs (frames that can pass
+// 2^55): its wait and the item's ticket are paid per item, so items are
+// larger there.
+constexpr int kItemPixelsFull = VMX_ITEM_PIXELS_FULL;
 constexpr int kUnroll = VMX_UNROLL;        // 16-byte vectors in flight per lane per plane
 #ifndef VMX_FLUSH_SAMPLES
 #define VMX_FLUSH_SAMPLES 256

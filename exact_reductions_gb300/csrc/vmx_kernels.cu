@@ -1523,19 +1523,18 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         }
         __syncwarp();
         // Lane 0 alone stores and adds the item's sums: a one-row item has
-        // them in lane 0 already. First-moment sums of an item fit 32 bits
-        // (at most 32768 samples below 2^16).
+        // them in lane 0 already. A lane's first-moment sum of an item fits
+        // 32 bits (at most 32 rows of 1024 samples below 2^16 a lane).
         Agg g = agg_zero();
         const bool one = r1 - r0 == 1;
         if (M) {
             g.s2[0] = one ? my_r : warp_sum_lt51(my_r);  // a row's sum is below 2^47
             g.s2[1] = one ? my_d : warp_sum_lt51(my_d);
-            g.s1[0] = warp_sum32(s1r);
-            g.s1[1] = warp_sum32(s1d);
+            g.s1[0] = warp_sum_lt51(s1r);
+            g.s1[1] = warp_sum_lt51(s1d);
         }
-        if (ODD && !one) {  // an item's counts fit 16 bits (at most 2^15 samples)
-            const uint32_t c = warp_sum32((uint32_t)my_o + ((uint32_t)(my_o >> 32) << 16));
-            g.odd = (uint64_t)(c & 0xffffu) | ((uint64_t)(c >> 16) << 32);
+        if (ODD && !one) {  // each count fits 32 bits
+            g.odd = (uint64_t)warp_sum32((uint32_t)my_o) | ((uint64_t)warp_sum32((uint32_t)(my_o >> 32)) << 32);
         } else if (ODD) {
             g.odd = my_o;
         }
