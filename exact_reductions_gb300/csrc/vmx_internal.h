@@ -11,10 +11,15 @@
 
 namespace vmx {
 
-constexpr int kThreads = 256;              // threads per CTA (8 independent warps)
+#ifndef VMX_THREADS
+#define VMX_THREADS 128
+#endif
+// Threads per CTA: four independent warps; six CTAs per SM. Small CTAs free
+// their slots early when the items run out, for the next call's kernel.
+constexpr int kThreads = VMX_THREADS;
 constexpr int kWarps = kThreads / 32;
 #ifndef VMX_MIN_BLOCKS
-#define VMX_MIN_BLOCKS 3
+#define VMX_MIN_BLOCKS 6
 #endif
 #ifndef VMX_UNROLL
 #define VMX_UNROLL 3
@@ -46,7 +51,7 @@ constexpr int kFlushSamples = VMX_FLUSH_SAMPLES; // 16-bit samples per lane and 
 #endif
 // Row chunks each warp keeps in shared memory, filled by bulk asynchronous
 // copies; 0 (the default): 16-byte loads straight into registers, which
-// measure faster on the 16-bit rows (with 3 stages and 2 CTAs per SM the
+// measure faster on the 16-bit rows (with 3 stages and 16 warps per SM the
 // 16-bit 3840x2160 batch takes about 9% longer).
 constexpr int kStages = VMX_STAGES;
 constexpr uint32_t kPipeSpinLimit = 1u << 20;  // polls of one chunk's barrier, at most

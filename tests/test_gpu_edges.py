@@ -74,6 +74,18 @@ def test_misaligned_past_2_55():
     run_and_check(ref, dis, 16, misalign=1)
 
 
+def test_past_2_55_ragged_last_items():
+    """Look-back items of several rows on frames whose height is not a
+    multiple of them (4000 wide: 9-row items, 2400 rows leave a 6-row last
+    item) past 2^55 units, so that the runs, the look-back and the walk meet
+    a short last item of every frame."""
+    rng = np.random.default_rng(31)
+    ref = rng.integers(60000, 65536, size=(2, 2400, 4000), dtype=np.uint16)
+    dis = rng.integers(60000, 65536, size=(2, 2400, 4000), dtype=np.uint16)
+    _, stats = run_and_check(ref, dis, 16)
+    assert int(stats[1]) > 0  # rows added by a closed form or a run
+
+
 def test_ragged_width_past_2_53():
     """A width that is not a multiple of 8 (a partial last vector) on a frame
     past 2^53 units: the crossing row walk reads the row's tail by samples."""
@@ -93,8 +105,8 @@ def test_widest_rows_largest_frame():
 
 
 def test_single_column_tall_frame():
-    """Width 1: every row is one term; frames of 2^21 + 1 pixels take the
-    look-back path with 64-row tiles."""
+    """Width 1: every row is one term; frames of 2^21 + 1 pixels count odd
+    terms, in items of 32 one-sample rows."""
     rng = np.random.default_rng(10)
     H = (1 << 21) + 1
     ref = rng.integers(60000, 65536, size=(1, H, 1), dtype=np.uint16)
