@@ -125,7 +125,7 @@ class FrameGraph:
     ``depth`` batches per replay, each with its own workspace and outputs
     (``self.outs[i]``; ``self.out`` is the last): the workspaces are cleared
     first, then the kernels run back to back, each launched to overlap the
-    end of the one before it (``vmx_frames_ex`` with ``VMX_FLAG_OVERLAP``).
+    one before it (``vmx_frames_ex`` with ``VMX_FLAG_OVERLAP``).
     ``refs``/``diss`` give each batch's input tensors (copy new frames into
     them between replays); by default every batch reads ``ref``/``dis``.
     Bounded device waits that give up are reported by ``status()``."""

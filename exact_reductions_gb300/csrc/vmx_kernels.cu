@@ -1451,6 +1451,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         }
         __syncwarp();
     }
+    // A kernel launched to overlap this one (the next call on the stream,
+    // which touches nothing this one writes) may be scheduled at once: its
+    // blocks take the SM slots this grid's blocks leave.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t nwarps = gridDim.x * (uint32_t)kWarps;
     const uint32_t gwarp = blockIdx.x * (uint32_t)kWarps + (threadIdx.x >> 5);
     const uint32_t first = FULL ? 0u : nwarps;  // tickets below are assigned
@@ -1467,12 +1471,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
             end = c + k;
         }
         const int tk = (int)cur++;
-        if (tk >= nitems) {
-            // Out of items: a kernel launched to overlap this one may start
-            // on the SMs that free up.
-            if (lane == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-            break;
-        }
+        if (tk >= nitems) break;
         int f, j;
         item_of_ticket(tk, p.frames, I, &f, &j);
         const int r0 = j * p.rows_per_item, r1 = min(H, r0 + p.rows_per_item);

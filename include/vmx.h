@@ -121,9 +121,9 @@ int vmx_moment_psnr_frames(const void *ref, const void *dis, int width, int heig
  *                     vmx_workspace_clear() did it on this stream since the
  *                     workspace was last used.
  *   VMX_FLAG_OVERLAP  launch the kernel so that it may start while the
- *                     previous kernel on `stream` is finishing (programmatic
- *                     dependent launch: on the SMs that kernel's blocks leave
- *                     once they have run out of work). The caller guarantees
+ *                     previous kernel on `stream` is still running
+ *                     (programmatic dependent launch: its blocks take the SM
+ *                     slots that kernel's blocks leave). The caller guarantees
  *                     that this call reads and writes nothing that kernel
  *                     writes (another workspace, other outputs) and that the
  *                     workspace was cleared beforehand (VMX_FLAG_CLEARED): a
