@@ -6,9 +6,9 @@ python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
 A step is one pass of the whole path (exact row sums, look-back, runs, walk,
 finalisation for both features) over one batch of 16 seeded synthetic frame
 pairs already resident in HBM: one library call on its own workspace and
-outputs. Steps run as a stream of batches does: CUDA graphs of four calls
+outputs. Steps run as a stream of batches does: CUDA graphs of sixteen calls
 (api.FrameGraph), the workspaces cleared first and each kernel launched to
-overlap the end of the one before it (programmatic dependent launch). The
+overlap the one before it (programmatic dependent launch). The
 batch (531 MB) is larger than L2. Under
 torchrun every rank runs its own batch on its own GPU (frames shard with no
 collective; weak scaling); rank 0 prints one JSON line. ``--impl
@@ -254,10 +254,10 @@ def run_ours(args, rank, local_rank, world, pg):
     ref = torch.from_numpy(ref_h).to(dev)
     dis = torch.from_numpy(dis_h).to(dev)
     # The step: one fused call on the resident batch. Steps go in CUDA graphs
-    # of `depth` calls (api.FrameGraph), each kernel launched to overlap the
-    # end of the one before it, as a stream of batches runs; every call does
-    # the whole work on its own workspace and outputs.
-    depth = 4 if args.steps % 4 == 0 else 1
+    # of `depth` calls (api.FrameGraph; 16 when the step count allows), each
+    # kernel launched to overlap the one before it, as a stream of batches
+    # runs; every call does the whole work on its own workspace and outputs.
+    depth = next(d for d in (16, 8, 4, 2, 1) if args.steps % d == 0)
     fg = api.FrameGraph(ref, dis, wl.bpc, features=3, depth=depth)
     stream = torch.cuda.current_stream(dev)
     kernels_per_step = 1
