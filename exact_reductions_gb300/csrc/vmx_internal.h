@@ -58,6 +58,9 @@ constexpr uint32_t kPipeSpinLimit = 1u << 20;  // polls of one chunk's barrier, 
 #ifndef VMX_G_DP2A
 #define VMX_G_DP2A 0
 #endif
+#ifndef VMX_LOW_DEPTH
+#define VMX_LOW_DEPTH 1
+#endif
 #ifndef VMX_WHOLE_LOADS
 #define VMX_WHOLE_LOADS 1
 #endif

@@ -410,6 +410,36 @@ __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
     }
 }
 
+// The same sums for a word pair whose four samples are all below 4096 (the
+// pass checked it): their binary32 squares, and those of their differences,
+// are exact, so there are no rounding errors to take off, and a term is odd
+// exactly when its sample is.
+template <bool M, bool P, bool ODD>
+__device__ __forceinline__ void acc16_word_low(Acc16 &a, uint32_t r, uint32_t d)
+{
+    if (M) {
+        const uint32_t xr = __byte_perm(r, 0, 0x3120), xd = __byte_perm(d, 0, 0x3120);
+        a.lr = __dp2a_lo(r, xr, a.lr);
+        a.hr = __dp2a_hi(r, xr, a.hr);
+        a.ld = __dp2a_lo(d, xd, a.ld);
+        a.hd = __dp2a_hi(d, xd, a.hd);
+        if (P) {
+            a.lx = __dp2a_lo(r, xd, a.lx);
+            a.hx = __dp2a_hi(r, xd, a.hx);
+        }
+        a.s1r = __dp2a_lo(r, 0x00000101u, a.s1r);
+        a.s1d = __dp2a_lo(d, 0x00000101u, a.s1d);
+        if (ODD) {
+            a.nzr = __dp2a_lo(~r & 0x00010001u, 0x00000101u, a.nzr);
+            a.nzd = __dp2a_lo(~d & 0x00010001u, 0x00000101u, a.nzd);
+        }
+    } else if (P) {
+        const int32_t i0 = (int32_t)(r & 0xffffu) - (int32_t)(d & 0xffffu);
+        const int32_t i1 = (int32_t)(r >> 16) - (int32_t)(d >> 16);
+        a.tp += (uint64_t)(i0 * i0) + (uint64_t)(i1 * i1);
+    }
+}
+
 // Folds the sums since the last flush into the row sums. At most
 // kFlushSamples (256) samples per lane and plane since the last flush keep
 // every dot-product sum below 2^32 (256 times 65535 times 255), every error
@@ -443,7 +473,10 @@ __device__ __forceinline__ void acc16_flush(Acc16 &a)
 // With STG the row's whole chunks come through the warp's chunk stream (the
 // row is the stream's next `cpr` chunks), the rest of the row straight from
 // global memory.
-template <bool M, bool P, bool ODD, bool VEC, bool STG>
+// With LOW (depths up to 12 bits) a pass whose samples are all below 4096
+// takes the exact-square body; any other pass (a container value past the
+// depth) the full one.
+template <bool M, bool P, bool ODD, bool VEC, bool STG, bool LOW>
 __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, int width, Pipe &pp,
                               const PipeSrc &src, uint32_t *status)
 {
@@ -512,13 +545,33 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
                 }
             }
         }
+        bool low = false;
+        if (LOW) {
+            uint32_t o = 0;
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            if (u < nu) {
-                acc16_word<M, P, ODD>(a, R[u].x, D[u].x);
-                acc16_word<M, P, ODD>(a, R[u].y, D[u].y);
-                acc16_word<M, P, ODD>(a, R[u].z, D[u].z);
-                acc16_word<M, P, ODD>(a, R[u].w, D[u].w);
+            for (int u = 0; u < kUnroll; ++u)
+                if (u < nu) o |= R[u].x | R[u].y | R[u].z | R[u].w | D[u].x | D[u].y | D[u].z | D[u].w;
+            low = !__any_sync(kFull, (o & 0xF000F000u) != 0u);
+        }
+        if (LOW && low) {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (u < nu) {
+                    acc16_word_low<M, P, ODD>(a, R[u].x, D[u].x);
+                    acc16_word_low<M, P, ODD>(a, R[u].y, D[u].y);
+                    acc16_word_low<M, P, ODD>(a, R[u].z, D[u].z);
+                    acc16_word_low<M, P, ODD>(a, R[u].w, D[u].w);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (u < nu) {
+                    acc16_word<M, P, ODD>(a, R[u].x, D[u].x);
+                    acc16_word<M, P, ODD>(a, R[u].y, D[u].y);
+                    acc16_word<M, P, ODD>(a, R[u].z, D[u].z);
+                    acc16_word<M, P, ODD>(a, R[u].w, D[u].w);
+                }
             }
         }
         pend += 8 * nu;
@@ -1419,7 +1472,7 @@ __device__ __forceinline__ void item_of_ticket(int tk, int F, int I, int *f, int
     }
 }
 
-template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC>
+template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC, bool LOW>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
 {
     const int lane = lane_id();
@@ -1493,7 +1546,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
             const unsigned char *rr = fr + (int64_t)r * p.stride;
             const unsigned char *dr = fd + (int64_t)r * p.stride;
             const RowSums rs = sizeof(TS) == 2
-                                   ? row_sums16<M, P, ODD, VEC, STG>(rr, dr, p.width, pp, src, p.status)
+                                   ? row_sums16<M, P, ODD, VEC, STG, LOW>(rr, dr, p.width, pp, src, p.status)
                                    : row_sums8<M, P, VEC>(rr, dr, p.width);
             if (lane == 0) {
                 if (M) {
@@ -1613,7 +1666,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
     if (p.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC>
+template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC, bool LOW>
 cudaError_t launch_one(const Params &p, const Layout &L, cudaStream_t stream)
 {
     static int blocks_per_sm[64] = {0};  // per device ordinal, filled once
@@ -1625,13 +1678,13 @@ cudaError_t launch_one(const Params &p, const Layout &L, cudaStream_t stream)
     const size_t smem = kStages > 0 && VEC && sizeof(TS) == 2 ? kPipeSmem : 0;
     if (blocks_per_sm[dev] == 0) {
         if (smem > 0) {
-            err = cudaFuncSetAttribute(frames_kernel<TS, M, P, ODD, FULL, VEC>,
+            err = cudaFuncSetAttribute(frames_kernel<TS, M, P, ODD, FULL, VEC, LOW>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (err != cudaSuccess) return err;
         }
         int n = 0;
         err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, frames_kernel<TS, M, P, ODD, FULL, VEC>, kThreads, smem);
+            &n, frames_kernel<TS, M, P, ODD, FULL, VEC, LOW>, kThreads, smem);
         if (err != cudaSuccess) return err;
         blocks_per_sm[dev] = n > 0 ? n : 1;
     }
@@ -1642,7 +1695,7 @@ cudaError_t launch_one(const Params &p, const Layout &L, cudaStream_t stream)
     const long long blocks = (warps + kWarps - 1) / kWarps;
     const int grid = (int)std::min<long long>(blocks, (long long)sms * blocks_per_sm[dev]);
     if (!p.overlap) {
-        frames_kernel<TS, M, P, ODD, FULL, VEC><<<grid, kThreads, smem, stream>>>(p);
+        frames_kernel<TS, M, P, ODD, FULL, VEC, LOW><<<grid, kThreads, smem, stream>>>(p);
         return cudaGetLastError();
     }
     // Programmatic dependent launch: may start once every block of the
@@ -1657,22 +1710,27 @@ cudaError_t launch_one(const Params &p, const Layout &L, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, frames_kernel<TS, M, P, ODD, FULL, VEC>, p);
+    return cudaLaunchKernelEx(&cfg, frames_kernel<TS, M, P, ODD, FULL, VEC, LOW>, p);
 }
 
-template <typename TS, bool M, bool P, bool ODD, bool FULL>
+template <typename TS, bool M, bool P, bool ODD, bool FULL, bool LOW = false>
 cudaError_t launch_vec(const Params &p, const Layout &L, bool vec, cudaStream_t s)
 {
-    return vec ? launch_one<TS, M, P, ODD, FULL, true>(p, L, s)
-               : launch_one<TS, M, P, ODD, FULL, false>(p, L, s);
+    return vec ? launch_one<TS, M, P, ODD, FULL, true, LOW>(p, L, s)
+               : launch_one<TS, M, P, ODD, FULL, false, LOW>(p, L, s);
 }
 
 template <bool M, bool P>
 cudaError_t launch_u16(const Params &p, const Layout &L, bool vec, cudaStream_t s)
 {
+    // Depths up to 12 bits check each pass for samples below 4096.
+    const bool low = VMX_LOW_DEPTH && L.bpc <= 12;
     if (L.full) return launch_vec<uint16_t, M, P, true, true>(p, L, vec, s);
-    if (L.ordered) return launch_vec<uint16_t, M, P, true, false>(p, L, vec, s);
-    return launch_vec<uint16_t, M, P, false, false>(p, L, vec, s);
+    if (L.ordered)
+        return low ? launch_vec<uint16_t, M, P, true, false, true>(p, L, vec, s)
+                   : launch_vec<uint16_t, M, P, true, false>(p, L, vec, s);
+    return low ? launch_vec<uint16_t, M, P, false, false, true>(p, L, vec, s)
+               : launch_vec<uint16_t, M, P, false, false>(p, L, vec, s);
 }
 
 }  // namespace
@@ -1688,7 +1746,8 @@ cudaError_t launch_frames(const Params &p, const Layout &L, int features, bool v
     }
     if (m && ps) return launch_u16<true, true>(p, L, vec, stream);
     if (m) return launch_u16<true, false>(p, L, vec, stream);
-    return launch_vec<uint16_t, false, true, false, false>(p, L, vec, stream);
+    return VMX_LOW_DEPTH && L.bpc <= 12 ? launch_vec<uint16_t, false, true, false, false, true>(p, L, vec, stream)
+                       : launch_vec<uint16_t, false, true, false, false>(p, L, vec, stream);
 }
 
 // Scratch of vmx_frames_noalloc: a fixed array in the module's static device

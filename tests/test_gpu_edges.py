@@ -74,6 +74,28 @@ def test_misaligned_past_2_55():
     run_and_check(ref, dis, 16, misalign=1)
 
 
+@pytest.mark.parametrize("bpc", [10, 12])
+def test_low_depths_with_container_values_past_the_depth(bpc):
+    """Depths up to 12 bits take an exact-square pass while every sample in
+    it is below 4096. Container values past the depth (up to 65535) must send
+    their passes through the full body: here mixed within rows and across
+    rows, and, at 3.7 M pixels, a frame whose rows past 2^53 units (their odd
+    terms counted on the exact-square passes) follow overrange rows."""
+    rng = np.random.default_rng(40 + bpc)
+    top = 1 << bpc
+    ref = rng.integers(0, top, size=(2, 64, 3000)).astype(np.uint16)
+    dis = rng.integers(0, top, size=(2, 64, 3000)).astype(np.uint16)
+    ref[:, ::3, :700] = rng.integers(4096, 65536, size=ref[:, ::3, :700].shape)
+    dis[:, 1::3, 1500:1510] = 65535
+    run_and_check(ref, dis, bpc)
+    H, W = 1440, 2560
+    ref = rng.integers(0, top, size=(1, H, W)).astype(np.uint16)
+    dis = rng.integers(0, top, size=(1, H, W)).astype(np.uint16)
+    ref[:, :1008] = rng.integers(60000, 65536, size=(1, 1008, W))
+    _, stats = run_and_check(ref, dis, bpc)
+    assert int(stats[1]) > 0  # rows past 2^53 added by a closed form
+
+
 def test_past_2_55_ragged_last_items():
     """Look-back items of several rows on frames whose height is not a
     multiple of them (4000 wide: 9-row items, 2400 rows leave a 6-row last
