@@ -238,7 +238,8 @@ VMX_HD Run lane_to_run(const LaneRun &r, uint64_t exact)
     return out;
 }
 
-// The compact run of n <= 8 terms under last place u = 2^sh, 1 <= sh <= 20.
+// The compact run of n terms under last place u = 2^sh, sh >= 1, while
+// n * 2u < 2^22 (the device forms 24-term runs in the same way).
 //
 // Only t mod 2u matters for how a term rounds: writing t = 2u*m + v with
 // 0 <= v < 2u, the increment is 2u*m plus the rounded increment of v from the
@@ -247,7 +248,7 @@ VMX_HD Run lane_to_run(const LaneRun &r, uint64_t exact)
 // place exactly u, and F + v rounds to the nearest multiple of u, a tie to the
 // even F / u, which is the CPU's rule with F / u standing for S / u. The even
 // trajectory starts at 1.5 * 2^23 * u (F / u even), the odd one a place
-// higher; eight adds of v < 2u never leave the binade.
+// higher; n adds of v < 2u never leave the binade while n * 2u < 2^22.
 VMX_HD LaneRun lane_run_fp(const uint32_t *t, int n, int sh)
 {
     const float uf = as_float((uint32_t)(127 + sh) << 23);  // 2^sh
