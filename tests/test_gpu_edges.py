@@ -87,7 +87,8 @@ def test_low_depths_with_container_values_past_the_depth(bpc):
     dis = rng.integers(0, top, size=(2, 64, 3000)).astype(np.uint16)
     ref[:, ::3, :700] = rng.integers(4096, 65536, size=ref[:, ::3, :700].shape)
     dis[:, 1::3, 1500:1510] = 65535
-    run_and_check(ref, dis, bpc)
+    for features in (3, 1, 2):
+        run_and_check(ref, dis, bpc, features=features)
     H, W = 1440, 2560
     ref = rng.integers(0, top, size=(1, H, W)).astype(np.uint16)
     dis = rng.integers(0, top, size=(1, H, W)).astype(np.uint16)
