@@ -61,6 +61,10 @@ constexpr uint32_t kPipeSpinLimit = 1u << 20;  // polls of one chunk's barrier, 
 #ifndef VMX_LOW_DEPTH
 #define VMX_LOW_DEPTH 1
 #endif
+#ifndef VMX_FIRST_UNROLL
+#define VMX_FIRST_UNROLL 16
+#endif
+constexpr int kFirstUnroll = VMX_FIRST_UNROLL;  // loads in flight per lane in the walks' sequential sums
 #ifndef VMX_WHOLE_LOADS
 #define VMX_WHOLE_LOADS 1
 #endif

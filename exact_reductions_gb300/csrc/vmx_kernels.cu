@@ -799,7 +799,7 @@ __device__ int warp_first(Fetch fetch, int lo, int hi, Bad bad, SC *before, uint
             return __shfl_sync(kFull, cand, src);
         }
         SC loc{0, 0};
-#pragma unroll 4
+#pragma unroll kFirstUnroll
         for (int i = a; i < b; ++i) loc = sc_add(loc, fetch(i));
         SC tot;
         const SC ex = warp_excl_sc(loc, &tot);
