@@ -55,18 +55,15 @@ constexpr int kFlushSamples = VMX_FLUSH_SAMPLES; // 16-bit samples per lane and 
 // 16-bit 3840x2160 batch takes about 9% longer).
 constexpr int kStages = VMX_STAGES;
 constexpr uint32_t kPipeSpinLimit = 1u << 20;  // polls of one chunk's barrier, at most
-#ifndef VMX_G_DP2A
-#define VMX_G_DP2A 0
-#endif
 #ifndef VMX_LOW_DEPTH
-#define VMX_LOW_DEPTH 1
+#define VMX_LOW_DEPTH 1  // depths up to 12 bits: exact-square passes where samples allow
 #endif
 #ifndef VMX_FIRST_UNROLL
 #define VMX_FIRST_UNROLL 16
 #endif
 constexpr int kFirstUnroll = VMX_FIRST_UNROLL;  // loads in flight per lane in the walks' sequential sums
 #ifndef VMX_WHOLE_LOADS
-#define VMX_WHOLE_LOADS 1
+#define VMX_WHOLE_LOADS 1  // passes wholly inside a row load without per-vector checks
 #endif
 constexpr uint32_t kSpinLimit = 1u << 22;  // bounded look-back wait (polls)
 

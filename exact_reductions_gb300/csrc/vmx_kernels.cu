@@ -67,17 +67,6 @@ __device__ __forceinline__ void st_release(uint32_t *ptr, uint32_t v)
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
-// Adds v at GPU scope with acquire-release order; returns the old value.
-__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *ptr, uint32_t v)
-{
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
-                 : "=r"(old)
-                 : "l"(ptr), "r"(v)
-                 : "memory");
-    return old;
-}
-
 // Adds v at GPU scope with release order (no value returned).
 __device__ __forceinline__ void red_add_release(uint64_t *ptr, uint64_t v)
 {
@@ -329,6 +318,11 @@ __device__ __forceinline__ Run warp_excl_run(const Run &x, int sh, Run *total)
 
 // --------------------------------------------------- phase A: row sums ---
 
+// A row's sums as the warp keeps them in shared memory for its item.
+struct alignas(32) RowSlot {
+    uint64_t x, y, z, w;  // ref and dis second-moment sums, psnr sum, odd counts (ref | dis << 32)
+};
+
 struct RowSums {
     uint64_t t2r, t2d, tp, s1r, s1d;
     uint32_t oddr, oddd;
@@ -367,13 +361,8 @@ __device__ __forceinline__ uint32_t halfword_min1(uint32_t x) { return __vminu2(
 template <bool M, bool P, bool ODD>
 __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
 {
-#if VMX_G_DP2A
-    const uint32_t gr0 = __dp2a_lo(r, 0x00000001u, kA), gr1 = __dp2a_lo(r, 0x00000100u, kA);
-    const uint32_t gd0 = __dp2a_lo(d, 0x00000001u, kA), gd1 = __dp2a_lo(d, 0x00000100u, kA);
-#else
     const uint32_t gr0 = __byte_perm(r, kA, 0x7610), gr1 = __byte_perm(r, kA, 0x7632);
     const uint32_t gd0 = __byte_perm(d, kA, 0x7610), gd1 = __byte_perm(d, kA, 0x7632);
-#endif
     const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
     const float2 fr = __fadd2_rn(make_float2(__uint_as_float(gr0), __uint_as_float(gr1)), m23);
     const float2 fd = __fadd2_rn(make_float2(__uint_as_float(gd0), __uint_as_float(gd1)), m23);
@@ -1488,7 +1477,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
     // would run one after another. Waits stay deadlock-free: a warp works
     // through its chunk in order, so the smallest unfinished item is always
     // some warp's current item.
-    __shared__ ulonglong4 item_rows[kWarps][kMaxRowsPerItem];  // sums of an item's rows
+    __shared__ RowSlot item_rows[kWarps][kMaxRowsPerItem];  // sums of an item's rows
     const int wid = (int)(threadIdx.x >> 5);
     // 16-bit rows on 16-byte boundaries stream through shared memory.
     constexpr bool STG = kStages > 0 && VEC && sizeof(TS) == 2;
@@ -1561,13 +1550,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
             }
             s1r += (uint32_t)rs.s1r;
             s1d += (uint32_t)rs.s1d;
-            if (lane == 0) item_rows[wid][r - r0] = make_ulonglong4(rs.t2r, rs.t2d, rs.tp,
-                                                                    (uint64_t)rs.oddr | ((uint64_t)rs.oddd << 32));
+            if (lane == 0)
+                item_rows[wid][r - r0] = RowSlot{rs.t2r, rs.t2d, rs.tp, (uint64_t)rs.oddr | ((uint64_t)rs.oddd << 32)};
         }
         __syncwarp();
         uint64_t my_r = 0, my_d = 0, my_p = 0, my_o = 0;  // this lane's row of the item
         if (lane < r1 - r0) {
-            const ulonglong4 v = item_rows[wid][lane];
+            const RowSlot v = item_rows[wid][lane];
             my_r = v.x;
             my_d = v.y;
             my_p = v.z;
