@@ -66,6 +66,11 @@ def _bind(path: str) -> ctypes.CDLL:
     lib.vmx_oracle_psnr_batch.restype = None
     lib.vmx_oracle_second_moment_lanes.argtypes = [vp, i32, i32, i64, i32, i32]
     lib.vmx_oracle_second_moment_lanes.restype = ctypes.c_double
+    lib.vmx_oracle_integer_psnr.argtypes = [vp, vp, i32, i32, i64, i32, u64p, u64p, dp]
+    lib.vmx_oracle_integer_psnr.restype = None
+    lib.vmx_oracle_integer_psnr_batch.argtypes = [vp, vp, i32, i32, i64, i32, i32, i32, u64p,
+                                                  u64p, dp]
+    lib.vmx_oracle_integer_psnr_batch.restype = None
     lib.vmx_oracle_mutation.argtypes = []
     lib.vmx_oracle_mutation.restype = i32
     return lib
@@ -161,6 +166,40 @@ def psnr(ref: np.ndarray, dis: np.ndarray, bpc: int, mutation: int = 0,
                         rows.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
                         ctypes.byref(mse))
     return rows, mse.value
+
+
+def integer_psnr(ref: np.ndarray, dis: np.ndarray, bpc: int, mutation: int = 0,
+                 width: Optional[int] = None) -> Tuple[np.ndarray, int, float]:
+    """integer_psnr of one plane pair: (exact row sums [height] of squared
+    codeword differences, the plane's sum, mse in codeword units)."""
+    lib = load(mutation)
+    pr, pd, w, h, s = _plane_args(ref, dis, width)
+    rows = np.zeros(h, dtype=np.uint64)
+    sse = ctypes.c_uint64(0)
+    mse = ctypes.c_double(0.0)
+    lib.vmx_oracle_integer_psnr(pr, pd, w, h, s, bpc,
+                                rows.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
+                                ctypes.byref(sse), ctypes.byref(mse))
+    return rows, int(sse.value), mse.value
+
+
+def integer_psnr_batch(ref: np.ndarray, dis: np.ndarray, bpc: int,
+                       width: Optional[int] = None):
+    """integer_psnr over a (F, H, W) batch: dict with ``rows`` [F][H],
+    ``sse`` [F], ``mse`` [F]."""
+    lib = load(0)
+    ref = np.ascontiguousarray(ref)
+    dis = np.ascontiguousarray(dis)
+    F, h, ss = ref.shape
+    w = ss if width is None else width
+    rows = np.zeros((F, h), dtype=np.uint64)
+    sse = np.zeros(F, dtype=np.uint64)
+    mse = np.zeros(F, dtype=np.float64)
+    u64 = ctypes.POINTER(ctypes.c_uint64)
+    lib.vmx_oracle_integer_psnr_batch(ref.ctypes.data, dis.ctypes.data, w, h, ref.strides[1],
+                                      bpc, 0, F, rows.ctypes.data_as(u64), sse.ctypes.data_as(u64),
+                                      mse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    return {"rows": rows, "sse": sse, "mse": mse}
 
 
 def psnr_db(mse: float, bpc: int, psnr_max: float = 0.0, mutation: int = 0) -> float:

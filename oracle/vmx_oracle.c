@@ -280,6 +280,55 @@ void vmx_oracle_psnr(const void *ref, const void *dis, int width, int height,
 #endif
 }
 
+/* integer_psnr of one plane pair (psnr_y, psnr_cb, psnr_cr each take one;
+ * the page on the Metal kernel batch T8-1c..k, "Feature scope" and "Integer
+ * kernels": integer partials, reduced in double on the host). The pages give
+ * no formula; the reading taken is the plain one: the sum of squared
+ * codeword differences, an exact integer per row and per plane (no
+ * normalisation, no rounding), and the MSE that sum divided by the pixel
+ * count in double. */
+void vmx_oracle_integer_psnr(const void *ref, const void *dis, int width, int height,
+                             int64_t stride_bytes, int bpc, uint64_t *rows, uint64_t *sse,
+                             double *mse)
+{
+    uint64_t total = 0;
+    for (int i = 0; i < height; ++i) {
+        const unsigned char *rr = row_ptr(ref, stride_bytes, i);
+        const unsigned char *dr = row_ptr(dis, stride_bytes, i);
+        uint64_t row = 0;
+        for (int j = 0; j < last_column(width); ++j) {
+            const int64_t d = (int64_t)sample_at(rr, j, bpc) - (int64_t)sample_at(dr, j, bpc);
+#if ORACLE_MUTATION == 14
+            row += (uint64_t)(d < 0 ? -d : d);
+#else
+            row += (uint64_t)(d * d);
+#endif
+        }
+        if (rows)
+            rows[i] = row;
+        total += row;
+    }
+    *sse = total;
+#if ORACLE_MUTATION == 15
+    *mse = (double)total / (double)width;
+#else
+    *mse = (double)total / pixel_count(width, height);
+#endif
+}
+
+void vmx_oracle_integer_psnr_batch(const void *ref, const void *dis, int width, int height,
+                                   int64_t stride_bytes, int bpc, int first, int count,
+                                   uint64_t *rows, uint64_t *sse, double *mse)
+{
+    const int64_t pitch = (int64_t)height * stride_bytes;
+    for (int f = 0; f < count; ++f) {
+        const int64_t off = (int64_t)(first + f) * pitch;
+        vmx_oracle_integer_psnr((const unsigned char *)ref + off, (const unsigned char *)dis + off,
+                                width, height, stride_bytes, bpc,
+                                rows ? rows + (size_t)f * height : NULL, sse + f, mse + f);
+    }
+}
+
 /* PSNR from the MSE. The pages leave the formula open; this is the reading
  * taken: the peak is the largest codeword on the 8-bit scale, the MSE is
  * floored at 1e-10, and the result is capped only when psnr_max > 0. */

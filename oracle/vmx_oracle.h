@@ -41,6 +41,17 @@ double vmx_oracle_psnr_noise(const void *ref, const void *dis, int width, int he
 void vmx_oracle_psnr(const void *ref, const void *dis, int width, int height,
                      int64_t stride_bytes, int bpc, uint64_t *rows, double *mse);
 
+/* integer_psnr of one plane pair: rows[height] (may be NULL) receives each
+ * row's exact sum of squared codeword differences, *sse the plane's, and
+ * *mse that sum divided by the pixel count (codeword units). */
+void vmx_oracle_integer_psnr(const void *ref, const void *dis, int width, int height,
+                             int64_t stride_bytes, int bpc, uint64_t *rows, uint64_t *sse,
+                             double *mse);
+void vmx_oracle_integer_psnr_batch(const void *ref, const void *dis, int width, int height,
+                                   int64_t stride_bytes, int bpc, int first, int count,
+                                   uint64_t *rows /* [count][height] or NULL */,
+                                   uint64_t *sse /* [count] */, double *mse /* [count] */);
+
 /* PSNR from the mean squared error on the 8-bit scale:
  * 10 * log10(peak^2 / max(mse, 1e-10)), peak = (2^bpc - 1) / 2^(bpc - 8),
  * capped at psnr_max when psnr_max > 0. */

@@ -194,6 +194,51 @@ def pin_psnr_closed_form(mutation=0):
     assert oracle.psnr_db(650.25, 8, 0.0, mutation=mutation) == 20.0
 
 
+def pin_integer_psnr_bruteforce(mutation=0, seeds=range(12)):
+    """integer_psnr against exact integer brute force in numpy: every row's
+    sum of squared codeword differences, the plane's sum and the MSE (the
+    sum, converted to double once, over the pixel count), on random planes
+    of every depth, including container values past the depth and padded
+    strides."""
+    for s in seeds:
+        rng = np.random.default_rng(900 + s)
+        bpc = [8, 10, 12, 16][s % 4]
+        h, w = int(rng.integers(1, 9)), int(rng.integers(1, 40))
+        mode = ["uniform", "extreme", "small", "overrange"][(s // 4) % 4]
+        ref, dis = synth.random_plane_pair(rng, w, h, bpc, stride_samples=w + 3, mode=mode)
+        rows, sse, mse = oracle.integer_psnr(ref, dis, bpc, mutation=mutation, width=w)
+        d = ref[:, :w].astype(np.int64) - dis[:, :w].astype(np.int64)
+        want_rows = (d * d).sum(axis=1).astype(np.uint64)
+        assert np.array_equal(rows, want_rows), (s, rows, want_rows)
+        assert sse == int((d * d).sum()), s
+        assert mse == float(int((d * d).sum())) / float(w * h), s
+
+
+def pin_integer_psnr_closed_forms(mutation=0):
+    """Constant planes a and b: every row adds W (a - b)^2 and the MSE is
+    (a - b)^2 exactly; where every difference is below 4096 the squares are
+    exact in binary32, so the rows equal float_psnr's rows (both in units of
+    a codeword squared); a difference past 4096 makes them differ."""
+    for bpc, a, b in ((8, 255, 0), (10, 3, 1000), (16, 65535, 0), (16, 40000, 39000)):
+        dt = np.uint8 if bpc == 8 else np.uint16
+        ref = np.full((5, 7), a, dtype=dt)
+        dis = np.full((5, 7), b, dtype=dt)
+        rows, sse, mse = oracle.integer_psnr(ref, dis, bpc, mutation=mutation)
+        assert np.all(rows == 7 * (a - b) ** 2), (bpc, rows)
+        assert sse == 35 * (a - b) ** 2 and mse == float((a - b) ** 2), (bpc, sse, mse)
+    rng = np.random.default_rng(77)
+    ref = rng.integers(0, 4096, size=(6, 50)).astype(np.uint16)
+    dis = rng.integers(0, 4096, size=(6, 50)).astype(np.uint16)
+    irows, _, _ = oracle.integer_psnr(ref, dis, 16, mutation=mutation)
+    frows, _ = oracle.psnr(ref, dis, 16)
+    assert np.array_equal(irows, frows)
+    ref[2, 3], dis[2, 3] = 65535, 100  # 65435^2 needs more than 24 bits
+    irows, _, _ = oracle.integer_psnr(ref, dis, 16, mutation=mutation)
+    frows, _ = oracle.psnr(ref, dis, 16)
+    assert irows[2] != frows[2] and np.array_equal(np.delete(irows, 2), np.delete(frows, 2))
+
+
 ALL_PINS = [pin_tiny_bruteforce, pin_all_codewords, pin_8bit_exact,
             pin_first_moment_closed_form, pin_psnr_closed_form, pin_constructed_frames,
-            pin_psnr_row_order, pin_past_2_53_bruteforce]
+            pin_psnr_row_order, pin_past_2_53_bruteforce, pin_integer_psnr_bruteforce,
+            pin_integer_psnr_closed_forms]

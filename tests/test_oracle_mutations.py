@@ -25,6 +25,8 @@ MUTATIONS = {
     10: "psnr row accumulator not reset per row",
     11: "ref and dis outputs swapped",
     13: "mse divided in float",
+    14: "integer_psnr adds |d| instead of d^2",
+    15: "integer_psnr divides by the width only",
 }
 
 
