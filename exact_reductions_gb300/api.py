@@ -199,6 +199,41 @@ class FrameGraph:
         return 0
 
 
+def integer_psnr(ref: torch.Tensor, dis: torch.Tensor, bpc: int, width: Optional[int] = None,
+                 rows: bool = False) -> Dict[str, torch.Tensor]:
+    """integer_psnr of a batch of one plane (luma or one chroma plane).
+
+    Returns device tensors ``sse`` [F] (uint64: exact sums of squared
+    codeword differences), ``mse`` [F] (sse / pixels) and, when asked,
+    ``rows`` [F, H]. PSNR in dB: ``integer_psnr_db(mse, bpc)``."""
+    lib = _lib.load()
+    ref, dis, F, H, W, stride = _geometry(ref, dis, bpc, width)
+    dev = ref.device
+    out = {"sse": torch.empty((F,), dtype=torch.uint64, device=dev),
+           "mse": torch.empty((F,), dtype=torch.float64, device=dev)}
+    if rows:
+        out["rows"] = torch.empty((F, H), dtype=torch.uint64, device=dev)
+    status = lib.vmx_integer_psnr_frames(ref.data_ptr(), dis.data_ptr(), W, H, stride, bpc, F,
+                                         _ptr(out["sse"]), _ptr(out["mse"]), _ptr(out.get("rows")),
+                                         _stream(dev))
+    _lib.check(status, "vmx integer_psnr")
+    return out
+
+
+def integer_psnr_planes(planes: Dict[str, tuple], bpc: int) -> Dict[str, Dict[str, torch.Tensor]]:
+    """integer_psnr of several planes, e.g. ``{"y": (ref_y, dis_y), "cb": ...,
+    "cr": ...}`` (psnr_y, psnr_cb, psnr_cr): one call per plane, each with
+    its own shape."""
+    return {name: integer_psnr(r, d, bpc) for name, (r, d) in planes.items()}
+
+
+def integer_psnr_db(mse, bpc: int, psnr_max: float = 0.0) -> np.ndarray:
+    """PSNR in dB of integer_psnr MSE values (codeword units): the library's
+    reading of the formula on the 8-bit scale (the ratio is the same)."""
+    mse = np.asarray(mse, dtype=np.float64) / float(4 ** (bpc - 8))
+    return psnr_db(mse, bpc, psnr_max)
+
+
 def moment_frames(ref, dis, bpc, **kw) -> Dict[str, torch.Tensor]:
     return frames(ref, dis, bpc, features=_lib.FEATURE_MOMENT, **kw)
 

@@ -25,9 +25,9 @@ CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-CU_SOURCES = ["vmx_kernels.cu"]
+CU_SOURCES = ["vmx_kernels.cu", "vmx_intpsnr.cu"]
 CPP_SOURCES = ["vmx_abi.cpp"]
-HEADERS = ["ordsum.cuh", "vmx_internal.h"]
+HEADERS = ["ordsum.cuh", "vmx_internal.h", "vmx_intpsnr.h"]
 
 LIB = os.path.join(BUILD, "libvmx.so")
 MODEL = os.path.join(BUILD, "libvmx_model.so")

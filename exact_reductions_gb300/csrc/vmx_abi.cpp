@@ -14,6 +14,7 @@
 
 #include "vmx.h"
 #include "vmx_internal.h"
+#include "vmx_intpsnr.h"
 
 namespace vmx {
 
@@ -258,6 +259,37 @@ int vmx_float_psnr_frames(const void *ref, const void *dis, int width, int heigh
     const Outputs o{nullptr, nullptr, nullptr, rows, mse, noise_sums};
     return run_frames(ref, dis, width, height, stride_bytes, bpc, nframes, VMX_FEATURE_PSNR, o,
                       workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int vmx_integer_psnr_frames(const void *ref, const void *dis, int width, int height,
+                            int64_t stride_bytes, int bpc, int nframes, uint64_t *sse,
+                            double *mse, uint64_t *rows, void *stream)
+{
+    if (!ref || !dis || !sse || !mse) return VMX_EINVAL;
+    if (width < 1 || width > 32768 || height < 1 || nframes < 1 || bpc < 8 || bpc > 16)
+        return VMX_EINVAL;
+    if ((int64_t)width * height > (int64_t)1 << 25) return VMX_EINVAL;
+    if (stride_bytes < (int64_t)width * bytes_per_sample(bpc)) return VMX_EINVAL;
+    if (bpc > 8 && ((uintptr_t)ref % 2 || (uintptr_t)dis % 2 || stride_bytes % 2)) return VMX_EINVAL;
+    if (fail_at("launch")) {
+        std::snprintf(g_last_cuda, sizeof g_last_cuda, "injected launch failure");
+        return VMX_ECUDA;
+    }
+    IntPsnrArgs a;
+    a.ref = static_cast<const unsigned char *>(ref);
+    a.dis = static_cast<const unsigned char *>(dis);
+    a.width = width;
+    a.height = height;
+    a.frames = nframes;
+    a.stride = stride_bytes;
+    a.bytes = bytes_per_sample(bpc);
+    a.sse = sse;
+    a.mse = mse;
+    a.rows = rows;
+    const cudaError_t err = launch_integer_psnr(a, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err);
+    g_launches.fetch_add(2, std::memory_order_relaxed);
+    return VMX_OK;
 }
 
 int vmx_moment_psnr_frames(const void *ref, const void *dis, int width, int height,

@@ -88,6 +88,27 @@ int vmx_moment_frames(const void *ref, const void *dis, int width, int height,
                       size_t workspace_bytes, void *stream);
 
 /*
+ * integer_psnr of nframes plane pairs (the page on the Metal kernel batch
+ * T8-1c..k, "Feature scope": psnr_y, psnr_cb and psnr_cr, one call per plane;
+ * "Integer kernels": integer partials). The pages give no formula; the
+ * reading taken: the exact sum of squared codeword differences (no
+ * normalisation, no rounding) and the MSE in codeword units.
+ *   ref, dis    device planes as vmx_moment_frames() (a chroma plane passes its
+ *               own width, height and stride).
+ *   sse         device, [nframes] uint64: each plane's sum (cleared and
+ *               written by the call).
+ *   mse         device, [nframes] doubles: sse / (width * height).
+ *   rows        device or NULL, [nframes][height] uint64: each row's sum.
+ * PSNR in dB on the host: vmx_psnr_db(mse / 4^(bpc - 8), bpc, psnr_max) (the
+ * same peak-to-MSE ratio on the 8-bit scale). No workspace; asynchronous on
+ * `stream`. Errors: VMX_EINVAL (as vmx_moment_frames(); sse and mse required;
+ * nothing launched), VMX_ECUDA.
+ */
+int vmx_integer_psnr_frames(const void *ref, const void *dis, int width, int height,
+                            int64_t stride_bytes, int bpc, int nframes, uint64_t *sse,
+                            double *mse, uint64_t *rows, void *stream);
+
+/*
  * float_psnr of nframes frame pairs (ADR-1499).
  *   rows        device, [nframes][height] uint64: each row's exact sum of the
  *               binary32 squared differences in units of 1/scaler^2.

@@ -82,6 +82,15 @@ def test_argument_errors_launch_nothing(lib):
     assert lib.vmx_moment_frames(p, p, 4, 4, 8, 16, 1, p, None, None, aligned, 16, None) == E
     assert lib.vmx_frames_host(None, p, 4, 4, 8, 16, 1, 3, p, None, p, p, None, 0.0, 1, None, 0,
                                None) == E
+    # integer_psnr: null planes or outputs, stride, depth, odd uint16 stride, width, frames
+    assert lib.vmx_integer_psnr_frames(None, p, 4, 4, 8, 16, 1, p, p, None, None) == E
+    assert lib.vmx_integer_psnr_frames(p, p, 4, 4, 8, 16, 1, None, p, None, None) == E
+    assert lib.vmx_integer_psnr_frames(p, p, 4, 4, 8, 16, 1, p, None, None, None) == E
+    assert lib.vmx_integer_psnr_frames(p, p, 4, 4, 6, 16, 1, p, p, None, None) == E
+    assert lib.vmx_integer_psnr_frames(p, p, 4, 4, 8, 7, 1, p, p, None, None) == E
+    assert lib.vmx_integer_psnr_frames(p, p, 4, 4, 9, 16, 1, p, p, None, None) == E
+    assert lib.vmx_integer_psnr_frames(p, p, 32769, 1, 1 << 17, 16, 1, p, p, None, None) == E
+    assert lib.vmx_integer_psnr_frames(p, p, 4, 4, 8, 16, 0, p, p, None, None) == E
     assert lib.vmx_kernel_launches() == launches
 
 
@@ -91,6 +100,8 @@ def test_injected_launch_failure(lib, monkeypatch):
     p = (ctypes.addressof(buf) + 255) & ~255
     monkeypatch.setenv("VMX_TEST_FAIL_AT", "launch")
     st = lib.vmx_moment_frames(p, p, 4, 4, 8, 16, 1, p, None, None, p, 1 << 15, None)
+    assert st == _lib.VMX_ECUDA and b"injected" in lib.vmx_strerror(st)
+    st = lib.vmx_integer_psnr_frames(p, p, 4, 4, 8, 16, 1, p, p, None, None)
     assert st == _lib.VMX_ECUDA and b"injected" in lib.vmx_strerror(st)
     monkeypatch.setenv("VMX_TEST_FAIL_AT", "alloc")
     st = lib.vmx_moment_frames(p, p, 4, 4, 8, 16, 1, p, None, None, None, 0, None)
