@@ -293,6 +293,17 @@ void vmx_model_run_of_terms(const uint32_t *t, int n, int sh, uint64_t *out)
     out[3] = lr.inc[1];
 }
 
+// One compact lane run over all n terms at once (the device forms its lane
+// runs of 24 consecutive terms this way), converted to the full run.
+void vmx_model_lane_run(const uint32_t *t, int n, int sh, uint64_t *out)
+{
+    uint64_t exact = 0;
+    for (int k = 0; k < n; ++k) exact += t[k];
+    const Run r = lane_to_run(lane_run_fp(t, n, sh), exact);
+    out[0] = r.inc[0];
+    out[1] = r.inc[1];
+}
+
 uint64_t vmx_model_rnd53(uint64_t x) { return rnd53(x); }
 uint32_t vmx_model_term(uint32_t p) { return term_of_sample(p); }
 

@@ -34,6 +34,8 @@ def model():
         lib.vmx_model_ordered_terms.restype = u64
         lib.vmx_model_run_of_terms.argtypes = [vp, i32, i32, vp]
         lib.vmx_model_run_of_terms.restype = None
+        lib.vmx_model_lane_run.argtypes = [vp, i32, i32, vp]
+        lib.vmx_model_lane_run.restype = None
         lib.vmx_model_set_mutation.argtypes = [i32]
         lib.vmx_model_rnd53.argtypes = [u64]
         lib.vmx_model_rnd53.restype = u64
@@ -127,6 +129,38 @@ def test_run_semantics_against_rounded_adds():
             assert s < (2 << e)
             assert int(out[p]) == s - s0, (trial, p)
             assert int(out[2 + p]) == s - s0, (trial, p, "compact")
+
+
+def test_long_lane_runs_against_rounded_adds():
+    """A lane's compact run of 24 consecutive terms (the device's length)
+    formed in one pass, for last places 2^3..2^10 (binades 55..62, every
+    binade a 16-bit frame can reach): its increments are the CPU's rounded
+    adds from an even and an odd start (ADR-1497 "Decision")."""
+    rng = np.random.default_rng(8)
+    m = model()
+    for trial in range(600):
+        sh = 3 + trial % 8
+        e = 52 + sh
+        n = 24 if trial % 4 else int(rng.integers(1, 48))
+        kind = trial % 3
+        if kind == 0:
+            t = rng.integers(0, 2**32, size=n, dtype=np.uint64)
+        elif kind == 1:
+            t = rng.integers(0, 65536, size=n, dtype=np.uint64)
+            t = np.array([m.vmx_model_term(int(p)) for p in t.tolist()], dtype=np.uint64)
+        else:
+            t = rng.integers(0, 4 << sh, size=n, dtype=np.uint64)
+        t32 = t.astype(np.uint32)
+        out = np.zeros(2, dtype=np.uint64)
+        m.vmx_model_lane_run(t32.ctypes.data, n, sh, out.ctypes.data)
+        u = 1 << sh
+        for p in (0, 1):
+            s0 = (1 << e) + (2 * int(rng.integers(0, 2**40)) + p) * u
+            s = s0
+            for v in t32.tolist():
+                s = rnd53(s + v)
+            assert s < (2 << e)
+            assert int(out[p]) == s - s0, (trial, n, sh, p)
 
 
 def test_rnd53_and_terms():
