@@ -41,10 +41,15 @@ KERNEL_SOURCES = [os.path.join(ROOT, "exact_reductions_gb300", "csrc", f)
 
 
 def kernel_hash() -> str:
+    """Hash of the kernel sources' code: comments and whitespace stripped,
+    so that a comment edit does not retire the profiled traffic."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

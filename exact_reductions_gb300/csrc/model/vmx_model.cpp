@@ -3,7 +3,8 @@
 //
 // The CUDA kernels form the CPU's second-moment sum of a 16-bit plane in
 // steps: exact row sums, a per-row plan from their exact prefix, per-row runs
-// built from 8-term lane runs (lane_run_fp) composed in order, and a walk
+// built from lane runs (lane_run_fp; 8 terms here, 24 on the device, the
+// same algebra) composed in order, and a walk
 // that adds each row exactly, by its run, or term by term. This file runs the
 // same arithmetic (ordsum.cuh) sequentially so the tests can hold it against
 // the CPU oracle without a GPU, with real plans, deliberately wrong plans and

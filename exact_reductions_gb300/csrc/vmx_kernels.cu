@@ -3,8 +3,9 @@
 // CPU's rounded double sums reproduced value for value.
 //
 // One persistent kernel per call; every warp works on its own. A warp takes
-// an item (a few whole rows of one frame, both planes) from a ticket counter,
-// in frame-major row order, with no CTA barrier anywhere:
+// items (a few whole rows of one frame, both planes) from a ticket counter,
+// frame by frame, the batch's last frames row by row across frames, with no
+// CTA barrier anywhere:
 //
 //   A. It streams the item's rows once with coalesced 16-byte loads and forms
 //      each row's exact sums: first moments (sum of p), second-moment terms
@@ -16,16 +17,17 @@
 //      item's exact sums are published and the exact sum before the item is
 //      read by a decoupled look-back over the frame's earlier items (bounded
 //      wait). Rows planned in a binade from 55 up get their run (ADR-1497
-//      "Decision", third point) from 256-pixel segments of 32 lanes x 8
-//      samples, re-reading the rows just streamed (L2 hits).
-//   C. Items fold into blocks of 32 (the warp that finishes a block sums it).
-//      Warps that find no item left take frames to walk, each waiting for its
-//      frame's last block: each plane's rows are added exactly, in closed form
-//      (binades 53 and 54, from the row's exact sum and odd count), by their
-//      run (from 55 up), or term by term where a row crosses a binade; psnr
-//      adds the exact row sums in row order (ADR-1499 "Decision"). Crossings
-//      are found by two-level warp searches over per-lane ranges. It writes
-//      the doubles the CPU divides out.
+//      "Decision", third point) from passes of 32 lanes x 24 consecutive
+//      samples, re-reading the rows just streamed (mostly L2 hits).
+//   C. The item's sums go into its block's sums (32 items) by 64-bit
+//      reductions, then the block's count by a release reduction. Warps that
+//      find no item left take frames to walk: the crossing of 2^53 is found
+//      as soon as the blocks before it are complete, that row is walked term
+//      by term, and once the frame is complete each plane's later rows are
+//      added in closed form (binades 53 and 54, from the rows' exact sums and
+//      odd counts), by their runs (from 55 up), or term by term where a row
+//      crosses a binade; psnr adds the exact row sums in row order (ADR-1499
+//      "Decision"). It writes the doubles the CPU divides out.
 #include <climits>
 
 #include "vmx.h"
