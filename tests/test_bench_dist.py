@@ -64,3 +64,18 @@ def test_whole_job_rate():
     # Two ranks, 16 frames each, 10 steps, slowest rank 0.5 s: 640 frames/s.
     assert bench.whole_job_rate(2, 16, 10, 0.5) == 640.0
     assert bench.max_over_ranks(3.25, None) == 3.25
+
+
+def test_kernel_hash_ignores_comments(tmp_path, monkeypatch):
+    """The profiled traffic stays keyed to the kernel code: a comment or
+    whitespace edit keeps the hash, a code edit changes it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("int f(int x) { return x + 1; }  // one\n/* two */\n")
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", [str(src)])
+    h0 = bench.kernel_hash()
+    src.write_text("// a new comment\nint f(int x)\n{\n    return x + 1;  /* same code */\n}\n")
+    assert bench.kernel_hash() == h0
+    src.write_text("int f(int x) { return x + 2; }\n")
+    assert bench.kernel_hash() != h0
