@@ -125,6 +125,21 @@ def test_psnr_db_matches_oracle(lib):
             assert np.array_equal(out.view(np.uint64), want.view(np.uint64))
 
 
+def test_integer_psnr_db_is_the_same_ratio(lib):
+    """integer_psnr's PSNR: the MSE in codeword units over 4^(bpc - 8) goes
+    through the same host step, and equals the oracle's PSNR of that
+    normalised MSE bit for bit (the division by a power of two is exact)."""
+    from exact_reductions_gb300 import api
+    rng = np.random.default_rng(12)
+    for bpc in (8, 10, 12, 16):
+        mse = np.concatenate([[0.0, 1.0], rng.uniform(0, 4.0 ** bpc, 100)])
+        got = api.integer_psnr_db(mse, bpc)
+        want = np.array([oracle.psnr_db(m / 4.0 ** (bpc - 8), bpc) for m in mse])
+        assert np.array_equal(got.view(np.uint64), want.view(np.uint64)), bpc
+        peak = float((1 << bpc) - 1)
+        assert api.integer_psnr_db(np.array([peak * peak]), bpc)[0] == 0.0
+
+
 def test_host_traffic(lib):
     h2d, d2h = ctypes.c_uint64(), ctypes.c_uint64()
     lib.vmx_frames_host_traffic(3840, 2160, 7680, 16, 16, 3, 0, ctypes.addressof(h2d),
