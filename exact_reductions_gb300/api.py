@@ -4,7 +4,8 @@ Planes are CUDA tensors of shape (frames, height, stride_samples), dtype
 uint8 (8 bpc) or uint16 (9..16 bpc), rows ``stride_samples`` apart;
 ``width`` (default: the last dimension) is how many samples of each row
 count. Work runs on the current CUDA stream of the tensors' device. The
-PSNR (a host function of the MSE) is ``psnr_db``.
+PSNR (a host function of the MSE) is ``psnr_db`` (``integer_psnr_db`` for
+``integer_psnr``, one plane a call).
 """
 
 from __future__ import annotations

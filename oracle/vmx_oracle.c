@@ -1,5 +1,6 @@
 /*
- * vmx_oracle.c -- the plain CPU definition of float_moment and float_psnr.
+ * vmx_oracle.c -- the plain CPU definition of float_moment, float_psnr and
+ * integer_psnr.
  *
  * TEST INFRASTRUCTURE ONLY: the oracle the CUDA library is checked against.
  * Only the tests, the smoke check and the benchmark's CPU-baseline leg use
@@ -19,6 +20,10 @@
  *     sample difference, a row's squares added into a double (noise_line()),
  *     the rows added into one double in row order, then divided by the pixel
  *     count (ADR-1499 "Context" and "Decision").
+ *   - integer_psnr, one plane pair at a time (psnr_y, psnr_cb, psnr_cr): the
+ *     exact integer sum of squared codeword differences and that sum over
+ *     the pixel count (the Metal kernel batch page names the feature and its
+ *     integer partials; the formula is the plain reading).
  *
  * Build: -O2 -fno-fast-math -ffp-contract=off -fno-tree-vectorize, so that
  * every float product is rounded to binary32 on its own (no fused multiply-

@@ -1,5 +1,6 @@
 /*
- * vmx_oracle.h -- the plain CPU definition of float_moment and float_psnr.
+ * vmx_oracle.h -- the plain CPU definition of float_moment, float_psnr and
+ * integer_psnr.
  *
  * TEST INFRASTRUCTURE ONLY. This is the oracle the CUDA library is checked
  * against. Only the tests, the smoke check and the benchmark's CPU-baseline
