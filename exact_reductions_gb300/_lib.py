@@ -44,6 +44,7 @@ SIGNATURES = {
     "vmx_workspace_status": (_i32, [_vp, _vp]),
     "vmx_workspace_stats": (_i32, [_vp, _vp, _vp]),
     "vmx_psnr_db": (_i32, [_vp, _i32, _i32, _dbl, _vp]),
+    "vmx_integer_psnr_db": (_i32, [_vp, _i32, _i32, _dbl, _vp]),
     "vmx_host_workspace_bytes": (_sz, [_i32, _i32, _i64, _i32, _i32, _i32]),
     "vmx_frames_host": (_i32, [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
                                _vp, _dbl, _i32, _vp, _sz, _vp]),

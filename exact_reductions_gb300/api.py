@@ -229,10 +229,13 @@ def integer_psnr_planes(planes: Dict[str, tuple], bpc: int) -> Dict[str, Dict[st
 
 
 def integer_psnr_db(mse, bpc: int, psnr_max: float = 0.0) -> np.ndarray:
-    """PSNR in dB of integer_psnr MSE values (codeword units): the library's
-    reading of the formula on the 8-bit scale (the ratio is the same)."""
-    mse = np.asarray(mse, dtype=np.float64) / float(4 ** (bpc - 8))
-    return psnr_db(mse, bpc, psnr_max)
+    """PSNR in dB of integer_psnr MSE values (codeword units), computed by
+    ``vmx_integer_psnr_db`` on the host."""
+    mse = np.ascontiguousarray(np.asarray(mse, dtype=np.float64))
+    out = np.zeros_like(mse)
+    _lib.check(_lib.load().vmx_integer_psnr_db(mse.ctypes.data, mse.size, bpc, float(psnr_max),
+                                               out.ctypes.data), "vmx integer psnr")
+    return out
 
 
 def moment_frames(ref, dis, bpc, **kw) -> Dict[str, torch.Tensor]:

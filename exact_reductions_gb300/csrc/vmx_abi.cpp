@@ -4,7 +4,6 @@
 
 #include <algorithm>
 #include <atomic>
-#include <chrono>
 #include <climits>
 #include <cmath>
 #include <cstdio>
@@ -21,18 +20,6 @@ namespace vmx {
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
-
-// Launch numbers: distinct per launch and, starting from the clock and an
-// address of this library, unlike anything an earlier process left in the
-// same memory. Items carry the number of the launch that wrote them.
-uint64_t next_launch_number()
-{
-    static std::atomic<uint64_t> seq{
-        ((uint64_t)std::chrono::steady_clock::now().time_since_epoch().count() << 20) ^
-        (uint64_t)(uintptr_t)&g_launches};
-    const uint64_t v = seq.fetch_add(1, std::memory_order_relaxed);
-    return v ? v : seq.fetch_add(1, std::memory_order_relaxed);
-}
 thread_local char g_last_cuda[160] = "";
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -70,6 +57,17 @@ bool wait_stall_setting()
     return v && std::strcmp(v, "1") == 0;
 }
 
+// Tests of forward progress: VMX_TEST_GRID_MULT=n (2..16) launches n times
+// as many CTAs as the GPU holds at once, so that most of the grid starts only
+// as earlier CTAs exit.
+int grid_mult_setting()
+{
+    const char *v = std::getenv("VMX_TEST_GRID_MULT");
+    if (!v) return 1;
+    const long n = std::strtol(v, nullptr, 10);
+    return n >= 2 && n <= 16 ? (int)n : 1;
+}
+
 int bytes_per_sample(int bpc) { return bpc == 8 ? 1 : 2; }
 
 }  // namespace
@@ -102,10 +100,10 @@ bool make_layout(int width, int height, int bpc, int frames, int features, Layou
     L->blocks_per_frame = bpf;
     size_t off = 0;
     L->off_ctrl = off;
-    off = align256(off + (kCtrlWords + (L->full ? F * I : 0)) * sizeof(uint32_t));
+    off = align256(off + (kCtrlWords + F * B + F * I) * sizeof(uint32_t));
+    L->ctrl_bytes = off;
     L->off_blocks = off;
     off = align256(off + F * B * sizeof(Agg));
-    L->ctrl_bytes = off;
     L->off_items = off;
     off = align256(off + F * I * sizeof(Agg));
     L->off_item_inc = off;
@@ -129,6 +127,19 @@ struct Outputs {
     uint64_t *noise_sums;
 };
 
+// The checks of a frame call's planes, shape and outputs (no CUDA call):
+// VMX_OK with the workspace layout in *L, else VMX_EINVAL.
+int check_frames_args(const void *ref, const void *dis, int width, int height, int64_t stride,
+                      int bpc, int nframes, int features, const Outputs &o, Layout *L)
+{
+    if (!ref || !dis || !make_layout(width, height, bpc, nframes, features, L)) return VMX_EINVAL;
+    if (stride < (int64_t)width * bytes_per_sample(bpc)) return VMX_EINVAL;
+    if ((features & VMX_FEATURE_MOMENT) && !o.moments) return VMX_EINVAL;
+    if ((features & VMX_FEATURE_PSNR) && (!o.psnr_rows || !o.mse)) return VMX_EINVAL;
+    if (bpc > 8 && ((uintptr_t)ref % 2 || (uintptr_t)dis % 2 || stride % 2)) return VMX_EINVAL;
+    return VMX_OK;
+}
+
 // status: where a bounded wait that gave up is recorded; NULL for the
 // workspace's own status word (cleared with the other control words).
 int run_frames(const void *ref, const void *dis, int width, int height, int64_t stride,
@@ -139,14 +150,11 @@ int run_frames(const void *ref, const void *dis, int width, int height, int64_t 
     if (flags & ~(unsigned)(VMX_FLAG_CLEARED | VMX_FLAG_OVERLAP)) return VMX_EINVAL;
     if (flags && !workspace) return VMX_EINVAL;
     Layout L;
-    if (!ref || !dis || !make_layout(width, height, bpc, nframes, features, &L)) return VMX_EINVAL;
-    if (stride < (int64_t)width * bytes_per_sample(bpc)) return VMX_EINVAL;
-    if ((features & VMX_FEATURE_MOMENT) && !o.moments) return VMX_EINVAL;
-    if ((features & VMX_FEATURE_PSNR) && (!o.psnr_rows || !o.mse)) return VMX_EINVAL;
-    if (bpc > 8 && ((uintptr_t)ref % 2 || (uintptr_t)dis % 2 || stride % 2)) return VMX_EINVAL;
+    const int bad = check_frames_args(ref, dis, width, height, stride, bpc, nframes, features, o, &L);
+    if (bad != VMX_OK) return bad;
     const bool own = workspace == nullptr;
     if (!own && (workspace_bytes < L.total || (uintptr_t)workspace % 256)) return VMX_EINVAL;
-    if (fail_at("alloc")) return VMX_ENOMEM;
+    if (own && fail_at("alloc")) return VMX_ENOMEM;
     if (fail_at("launch")) {
         std::snprintf(g_last_cuda, sizeof g_last_cuda, "injected launch failure");
         return VMX_ECUDA;
@@ -172,7 +180,8 @@ int run_frames(const void *ref, const void *dis, int width, int height, int64_t 
     p.items_per_frame = L.items_per_frame;
     p.blocks_per_frame = L.blocks_per_frame;
     p.ctrl = reinterpret_cast<uint32_t *>(ws + L.off_ctrl);
-    p.flags = p.ctrl + kCtrlWords;
+    p.block_fin = p.ctrl + kCtrlWords;
+    p.flags = p.block_fin + (size_t)nframes * L.blocks_per_frame;
     p.status = status_word ? status_word : p.ctrl + kCtrlStatus;
     p.items = reinterpret_cast<Agg *>(ws + L.off_items);
     p.blocks = reinterpret_cast<Agg *>(ws + L.off_blocks);
@@ -187,7 +196,7 @@ int run_frames(const void *ref, const void *dis, int width, int height, int64_t 
     p.noise_sums = o.noise_sums;
     p.spin_limit = spin_limit_setting();
     p.test_stall = wait_stall_setting() ? 1u : 0u;
-    p.launch = next_launch_number();
+    p.test_grid_mult = grid_mult_setting();
     p.overlap = (flags & VMX_FLAG_OVERLAP) ? 1u : 0u;
     const bool vec = (uintptr_t)ref % 16 == 0 && (uintptr_t)dis % 16 == 0 && stride % 16 == 0;
     err = (flags & VMX_FLAG_CLEARED) ? cudaSuccess
@@ -362,6 +371,20 @@ int vmx_psnr_db(const double *mse, int n, int bpc, double psnr_max, double *psnr
         double db = 10.0 * std::log10(peak * peak / m);
         if (psnr_max > 0.0 && db > psnr_max) db = psnr_max;
         psnr[i] = db;
+    }
+    return VMX_OK;
+}
+
+int vmx_integer_psnr_db(const double *mse, int n, int bpc, double psnr_max, double *psnr)
+{
+    if (!mse || !psnr || n < 0 || bpc < 8 || bpc > 16) return VMX_EINVAL;
+    // MSE in codeword units over 4^(bpc - 8) (a power of two: exact) is the
+    // MSE on the 8-bit scale that vmx_psnr_db takes.
+    const double scale = 1.0 / (double)(1ull << (2 * (bpc - 8)));
+    for (int i = 0; i < n; ++i) {
+        const double m = mse[i] * scale;
+        const int rc = vmx_psnr_db(&m, 1, bpc, psnr_max, psnr + i);
+        if (rc != VMX_OK) return rc;
     }
     return VMX_OK;
 }
@@ -589,9 +612,13 @@ int vmx_frames_noalloc(const void *ref, const void *dis, int width, int height,
                        uint64_t *psnr_rows, double *mse, uint64_t *noise_sums,
                        uint32_t *status, void *stream)
 {
-    // Shape checks first: nothing touches the device for a rejected shape.
+    // Every argument check first: nothing touches the device for a rejected
+    // call (the planes, the shape, the outputs, then the scratch limit).
     Layout L;
-    if (!make_layout(width, height, bpc, nframes, features, &L)) return VMX_EINVAL;
+    const Outputs o{moments, s2_rows, s2_sums, psnr_rows, mse, noise_sums};
+    const int bad = check_frames_args(ref, dis, width, height, stride_bytes, bpc, nframes, features,
+                                      o, &L);
+    if (bad != VMX_OK) return bad;
     if (L.total > VMX_NOALLOC_SCRATCH_BYTES) return VMX_ESCRATCH;
     int dev = -1;
     cudaError_t err = cudaGetDevice(&dev);
@@ -608,7 +635,6 @@ int vmx_frames_noalloc(const void *ref, const void *dis, int width, int height,
             g_noalloc_ptr[dev].store(ws, std::memory_order_release);
         }
     }
-    const Outputs o{moments, s2_rows, s2_sums, psnr_rows, mse, noise_sums};
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     // run_frames clears the control words (tickets, counters, the status
     // word) on `cs` before its launch; the rest of the scratch is written

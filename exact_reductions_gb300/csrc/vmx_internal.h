@@ -62,6 +62,24 @@ constexpr uint32_t kPipeSpinLimit = 1u << 20;  // polls of one chunk's barrier, 
 #define VMX_FIRST_UNROLL 16
 #endif
 constexpr int kFirstUnroll = VMX_FIRST_UNROLL;  // loads in flight per lane in the walks' sequential sums
+#ifndef VMX_S1_MODE
+#define VMX_S1_MODE 0  // first moments: 0 dot products, 1 packed adds, 2 SIMD absolute-difference sums
+#endif
+#ifndef VMX_ODD_MODE
+#define VMX_ODD_MODE 0  // even-term marks: 0 dot products, 1 packed adds, 2 SIMD minimum sums
+#endif
+#ifndef VMX_LOOP_MODE
+#define VMX_LOOP_MODE 0  // 1: passes wholly inside a row in a loop of their own
+#endif
+#ifndef VMX_PREFETCH
+#define VMX_PREFETCH 0  // passes ahead that each warp starts into L2 (0: none)
+#endif
+#ifndef VMX_SMEM_ACC
+#define VMX_SMEM_ACC 0  // 1: flush-only row sums in shared memory, first moments summed per row
+#endif
+#ifndef VMX_FOLD_MODE
+#define VMX_FOLD_MODE 0  // block counts: 0 acquire-release, 1 relaxed, 2 relaxed and looked at an item later
+#endif
 #ifndef VMX_WHOLE_LOADS
 #define VMX_WHOLE_LOADS 1  // passes wholly inside a row load without per-vector checks
 #endif
@@ -80,17 +98,17 @@ enum Ctrl : int {
 };
 
 // Per-item and per-block sums the walk reads (64 bytes): the exact
-// second-moment sums (ref, dis), the first-moment sums, the psnr sum, the
-// odd-term counts (ref in the low half of odd, dis in the high half) and, in
-// a block, how many of its items have added their sums; in an item, the
-// number of the launch that wrote it.
+// second-moment sums (ref, dis), the first-moment sums, the psnr sum and the
+// odd-term counts (ref in the low half of odd, dis in the high half). A
+// block's record is written by the block's last item to finish, from its
+// items' records. Whether a record is out is kept apart, in words cleared by
+// every call (an item's flag, a block's count of finished items).
 struct alignas(16) Agg {
     uint64_t s2[2];
     uint64_t s1[2];
     uint64_t psnr;
     uint64_t odd;
-    uint64_t count;
-    uint64_t pad;
+    uint64_t pad[2];
 };
 constexpr int kBlockItems = 32;  // items folded into one block aggregate
 
@@ -100,9 +118,9 @@ struct Layout {
     int rows_per_item, items_per_frame, blocks_per_frame;
     bool ordered;        // second moments may pass 2^53 units: odd counts per row
     bool full;           // ... and 2^55: look-back and row runs from binade 55 up
-    size_t off_ctrl;     // u32 [kCtrlWords] + flag[F * I]
-    size_t off_blocks;   // Agg [F * B], summed into by the items
-    size_t ctrl_bytes;   // bytes cleared per call: the control words and the blocks
+    size_t off_ctrl;     // u32 [kCtrlWords] + finished items per block [F * B] + item flags [F * I]
+    size_t ctrl_bytes;   // bytes cleared per call: the control words, counts and flags
+    size_t off_blocks;   // Agg [F * B], written by each block's last item
     size_t off_items;    // Agg [F * I]
     size_t off_item_inc; // u64 [F * I][2] inclusive exact prefix per item (look-back)
     size_t off_s2_rows;  // u64 [F][2][H] (when the caller passes none)
@@ -121,7 +139,9 @@ struct Params {
     int width, height, frames;
     int k;            // bpc - 8
     int rows_per_item, items_per_frame, blocks_per_frame;
-    uint32_t *ctrl, *flags;
+    uint32_t *ctrl;
+    uint32_t *flags;      // per item: 0, 1 (its record is out), 2 (and its inclusive prefix)
+    uint32_t *block_fin;  // items of each block that have finished (32-bit counts)
     uint32_t *status;  // set to 1 when a bounded wait gives up
     Agg *items, *blocks;
     uint64_t *item_inc;
@@ -131,9 +151,9 @@ struct Params {
     double *moments, *mse;
     uint64_t *s2_sums, *noise_sums;
     uint32_t spin_limit;
-    uint64_t launch;  // this launch's number (never 0): stamps finished items
     uint32_t overlap; // launched to overlap the previous kernel on the stream
     uint32_t test_stall;  // tests only: the walks wait for a count never reached
+    int test_grid_mult;   // tests only (host side): launch this many times the resident CTAs
 };
 
 // Enqueue the frame kernel. `features` VMX_FEATURE_* bits; `vec` true when

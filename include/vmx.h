@@ -99,10 +99,10 @@ int vmx_moment_frames(const void *ref, const void *dis, int width, int height,
  *               written by the call).
  *   mse         device, [nframes] doubles: sse / (width * height).
  *   rows        device or NULL, [nframes][height] uint64: each row's sum.
- * PSNR in dB on the host: vmx_psnr_db(mse / 4^(bpc - 8), bpc, psnr_max) (the
- * same peak-to-MSE ratio on the 8-bit scale). No workspace; asynchronous on
- * `stream`. Errors: VMX_EINVAL (as vmx_moment_frames(); sse and mse required;
- * nothing launched), VMX_ECUDA.
+ * PSNR in dB on the host: vmx_integer_psnr_db(). No workspace; asynchronous
+ * on `stream`. Errors: VMX_EINVAL (as vmx_moment_frames(); sse and mse
+ * required; nothing launched), VMX_ECUDA. Each row's sum goes into its
+ * plane's sum by a 64-bit integer atomic add (exact in any order).
  */
 int vmx_integer_psnr_frames(const void *ref, const void *dis, int width, int height,
                             int64_t stride_bytes, int bpc, int nframes, uint64_t *sse,
@@ -187,6 +187,16 @@ int vmx_workspace_stats(const void *workspace, void *stream, uint64_t *out4);
 int vmx_psnr_db(const double *mse, int n, int bpc, double psnr_max, double *psnr);
 
 /*
+ * PSNR in dB of integer_psnr MSE values (the page on the Metal kernel batch
+ * T8-1c..k, "Feature scope": psnr_y, psnr_cb, psnr_cr; no formula given):
+ * the MSE in codeword units over 4^(bpc - 8) (exact: a power of two), which
+ * is the MSE on the 8-bit scale, then vmx_psnr_db() of it. Host arrays of n
+ * doubles; psnr_max as vmx_psnr_db(). Errors: VMX_EINVAL (a NULL array,
+ * n < 0, bpc outside 8..16; nothing written).
+ */
+int vmx_integer_psnr_db(const double *mse, int n, int bpc, double psnr_max, double *psnr);
+
+/*
  * Host-memory entry point: frames in host memory, results in host memory,
  * same layout and outputs as the device calls, `chunk_frames` frames per
  * launch on `stream`. Page-locked (mapped) inputs are read in place by the
@@ -243,7 +253,8 @@ void vmx_frames_host_traffic(int width, int height, int64_t stride_bytes, int bp
  *               kernel to 0, or to 1 when a bounded device wait gave up (the
  *               outputs are then not valid).
  * Asynchronous on `stream`. Returns VMX_OK, VMX_EINVAL (arguments, as the
- * other calls), VMX_ESCRATCH, or VMX_ECUDA.
+ * other calls), VMX_ESCRATCH, or VMX_ECUDA. Every argument is checked, and
+ * VMX_EINVAL or VMX_ESCRATCH returned, before any CUDA call.
  */
 #define VMX_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 int vmx_frames_noalloc(const void *ref, const void *dis, int width, int height,

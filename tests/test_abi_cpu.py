@@ -126,18 +126,28 @@ def test_psnr_db_matches_oracle(lib):
 
 
 def test_integer_psnr_db_is_the_same_ratio(lib):
-    """integer_psnr's PSNR: the MSE in codeword units over 4^(bpc - 8) goes
-    through the same host step, and equals the oracle's PSNR of that
-    normalised MSE bit for bit (the division by a power of two is exact)."""
+    """integer_psnr's PSNR (vmx_integer_psnr_db, through the C ABI and the
+    binding): the MSE in codeword units over 4^(bpc - 8) goes through the
+    same host step, and equals the oracle's PSNR of that normalised MSE bit
+    for bit (the division by a power of two is exact)."""
     from exact_reductions_gb300 import api
     rng = np.random.default_rng(12)
     for bpc in (8, 10, 12, 16):
         mse = np.concatenate([[0.0, 1.0], rng.uniform(0, 4.0 ** bpc, 100)])
-        got = api.integer_psnr_db(mse, bpc)
-        want = np.array([oracle.psnr_db(m / 4.0 ** (bpc - 8), bpc) for m in mse])
-        assert np.array_equal(got.view(np.uint64), want.view(np.uint64)), bpc
+        for cap in (0.0, 60.0):
+            want = np.array([oracle.psnr_db(m / 4.0 ** (bpc - 8), bpc, cap) for m in mse])
+            out = np.zeros_like(mse)
+            assert lib.vmx_integer_psnr_db(mse.ctypes.data, mse.size, bpc, cap,
+                                           out.ctypes.data) == _lib.VMX_OK
+            assert np.array_equal(out.view(np.uint64), want.view(np.uint64)), (bpc, cap)
+            got = api.integer_psnr_db(mse, bpc, cap)
+            assert np.array_equal(got.view(np.uint64), want.view(np.uint64)), (bpc, cap)
         peak = float((1 << bpc) - 1)
         assert api.integer_psnr_db(np.array([peak * peak]), bpc)[0] == 0.0
+    x = np.zeros(1)
+    assert lib.vmx_integer_psnr_db(None, 1, 16, 0.0, x.ctypes.data) == _lib.VMX_EINVAL
+    assert lib.vmx_integer_psnr_db(x.ctypes.data, 1, 17, 0.0, x.ctypes.data) == _lib.VMX_EINVAL
+    assert lib.vmx_integer_psnr_db(x.ctypes.data, -1, 16, 0.0, x.ctypes.data) == _lib.VMX_EINVAL
 
 
 def test_host_traffic(lib):

@@ -269,3 +269,16 @@ def test_launch_counter_counts_calls():
     before = api.kernel_launches()
     run_and_check(ref, dis, 8)
     assert api.kernel_launches() == before + 1
+
+
+@pytest.mark.parametrize("key,frames", [("C4", 16), ("T2", 1), ("T4", 2)])
+def test_grid_larger_than_the_gpu_holds(monkeypatch, key, frames):
+    """Forward progress does not rest on the whole grid being resident at
+    once: with four times as many CTAs as the GPU holds (most of them start
+    only as earlier ones exit, and find no items left), the call comes back
+    with status 0 and every output equal to the oracle's. Items go out by
+    ticket only, so each item a walk waits for is held by a running warp."""
+    monkeypatch.setenv("VMX_TEST_GRID_MULT", "4")
+    wl = synth.WORKLOADS[key]
+    ref, dis = wl.batch(frames)
+    run_and_check(ref, dis, wl.bpc, frames=sorted({0, frames - 1}))

@@ -3,8 +3,9 @@
 The no-alloc call keeps its scratch in a fixed static device array; these
 tests run it twice in a row on each batch and hold every output to the
 workspace call's, bit for bit (the library's tolerance for every output is
-exact equality). The file is collected last so that it also runs after all
-other GPU tests in one process; it needs nothing they set up.
+exact equality), and the first and last frames straight to the oracle's.
+The file is collected last so that it also runs after all other GPU tests
+in one process; it needs nothing they set up.
 """
 
 import ctypes
@@ -30,6 +31,20 @@ def test_noalloc_rejects_without_touching_the_device():
     rc = lib.vmx_frames_noalloc(fake, fake, 0, 2160, 7680, 16, 1, 3, fake, None, None,
                                 fake, fake, None, None, None)
     assert rc == _lib.VMX_EINVAL
+    # Null planes, a short or odd stride, a missing output, a misaligned
+    # 16-bit plane: all argument errors, found before the device lookup (this
+    # test runs without a GPU, so any CUDA call would have failed otherwise).
+    odd = ctypes.c_void_p(257)
+    for args in [(None, fake, 64, 8, 128, 16, 1, 3, fake, None, None, fake, fake),
+                 (fake, None, 64, 8, 128, 16, 1, 3, fake, None, None, fake, fake),
+                 (fake, fake, 64, 8, 126, 16, 1, 3, fake, None, None, fake, fake),
+                 (fake, fake, 64, 8, 129, 16, 1, 3, fake, None, None, fake, fake),
+                 (fake, fake, 64, 8, 128, 16, 1, 3, None, None, None, fake, fake),
+                 (fake, fake, 64, 8, 128, 16, 1, 3, fake, None, None, None, fake),
+                 (fake, fake, 64, 8, 128, 16, 1, 3, fake, None, None, fake, None),
+                 (odd, fake, 64, 8, 128, 16, 1, 3, fake, None, None, fake, fake),
+                 (fake, fake, 64, 8, 128, 16, 1, 4, fake, None, None, fake, fake)]:
+        assert lib.vmx_frames_noalloc(*args, None, None, None) == _lib.VMX_EINVAL, args
     assert lib.vmx_kernel_launches() == before
 
 
@@ -37,6 +52,8 @@ def test_noalloc_rejects_without_touching_the_device():
 @pytest.mark.parametrize("key,frames", [("C2", 16), ("T1", 1), ("T2", 1), ("C4", 4)])
 def test_noalloc_matches_workspace_call(key, frames):
     import torch
+
+    from gpu_helpers import oracle_frames
 
     lib = _lib.load()
     wl = synth.WORKLOADS[key]
@@ -87,3 +104,17 @@ def test_noalloc_matches_workspace_call(key, frames):
             a = want[name].cpu().numpy().view(np.uint64)
             b = got[name].cpu().numpy().view(np.uint64)
             assert np.array_equal(a, b), (call, name)
+
+    # And straight against the oracle on the first and last frames.
+    for f, w in zip(sorted({0, F - 1}), oracle_frames(ref, dis, wl.bpc, sorted({0, F - 1}))):
+        m = got["moments"].cpu().numpy().reshape(F, 4)[f]
+        assert np.array_equal(m.view(np.uint64), w["moments"].view(np.uint64)), f
+        rows = got["s2_rows"].cpu().numpy().view(np.uint64).reshape(F, 2, H)[f]
+        assert np.array_equal(rows, w["s2_rows"]), f
+        sums = got["s2_sums"].cpu().numpy().view(np.uint64).reshape(F, 2)[f]
+        assert np.array_equal(sums, w["s2_sums"]), f
+        prow = got["psnr_rows"].cpu().numpy().view(np.uint64).reshape(F, H)[f]
+        assert np.array_equal(prow, w["psnr_rows"]), f
+        mse = got["mse"].cpu().numpy()[f]
+        assert np.array_equal(np.float64(mse).view(np.uint64), np.float64(w["mse"]).view(np.uint64)), f
+        assert int(got["noise_sums"].cpu().numpy().view(np.uint64)[f]) == w["noise_sum"], f
