@@ -35,7 +35,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "frames/s and achieved HBM GB/s (fraction of peak), 16-bit 3840x2160, bit-exact"
 WORKLOAD = "C4"
-PROFILE = os.path.join(ROOT, "profiles", "frames_kernel_c4.md")
+PROFILE = os.path.join(ROOT, "profiles", "frames_kernel_c4.json")
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, the vendor's figure (context only)
+GRAPH_DEPTH = 16          # calls per graph replay in the timed stream of batches
 KERNEL_SOURCES = [os.path.join(ROOT, "exact_reductions_gb300", "csrc", f)
                   for f in ("vmx_kernels.cu", "ordsum.cuh", "vmx_internal.h")]
 
@@ -68,17 +70,43 @@ def peak_hbm():
 
 
 def profiled_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, or None when the
-    summary is missing or was taken on other kernel sources."""
+    """Per-launch DRAM bytes from the committed ncu summary (a small JSON
+    record beside its text), or None when it is missing or was taken on other
+    kernel sources."""
     try:
-        text = open(PROFILE).read()
-    except OSError:
+        with open(PROFILE) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    h = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]+)", text)
-    if not m or not h or h.group(1) != kernel_hash():
+    if rec.get("kernel_sources_sha256_16") != kernel_hash():
         return None
-    return int(m.group(1))
+    v = rec.get("traffic_bytes_per_launch")
+    return int(v) if isinstance(v, int) else None
+
+
+def host_cpu():
+    """The host's CPU model and machine name, as the system reports them."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as fh:
+                for line in fh:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"cpu_model": model or platform.processor() or "unknown",
+            "uname_m": platform.machine()}
 
 
 class Clocks:
@@ -172,7 +200,9 @@ def make_batch(rank: int):
 
 def cpu_baseline(ref, dis, bpc, target_s: float = 2.0):
     """The oracle, as it stands, on the host cores: one frame per thread,
-    repeated until about target_s of wall time (bounded sample)."""
+    repeated until about target_s of wall time (bounded sample); then one
+    frame on one core, five times (median). Returns the baseline record and
+    the oracle's results of the frames it computed (moments, mse, psnr_rows)."""
     import oracle
     threads = os.cpu_count() or 1
     n = min(threads, ref.shape[0])
@@ -180,14 +210,83 @@ def cpu_baseline(ref, dis, bpc, target_s: float = 2.0):
     oracle.batch(sub_r[:1], sub_d[:1], bpc, threads=1)  # warm (build, page-in)
     done, t0 = 0, time.perf_counter()
     while True:
-        oracle.batch(sub_r, sub_d, bpc, threads=threads)
+        want = oracle.batch(sub_r, sub_d, bpc, threads=threads)
         done += n
         el = time.perf_counter() - t0
         if el >= target_s:
             break
-    return {"value": done / el, "unit": "frames/s", "cores": min(threads, n), "kind": "oracle",
-            "sample": f"{done} frame computations (float_moment + float_psnr) of the first {n} "
-                      f"frames of the workload, {min(threads, n)} threads, {el:.1f} s wall"}
+    one = []
+    for _ in range(5):
+        t1 = time.perf_counter()
+        oracle.batch(sub_r[:1], sub_d[:1], bpc, threads=1)
+        one.append(time.perf_counter() - t1)
+    rec = {"value": done / el, "unit": "frames/s", "cores": min(threads, n), "kind": "oracle",
+           "sample": f"{done} frame computations (float_moment + float_psnr) of the first {n} "
+                     f"frames of the workload, {min(threads, n)} threads, {el:.1f} s wall",
+           "single_thread_ms_per_frame": 1e3 * statistics.median(one),
+           "single_thread_sample": "frame 0, one thread, median of 5",
+           "pages_cpu_ms_per_frame": 17.0,
+           "pages_cpu_note": "the pages' CPU extractor on their unnamed host, 16-bit 3840x2160 "
+                             "(context only)"}
+    rec.update(host_cpu())
+    return rec, want
+
+
+def oracle_accumulators(ref, dis, bpc, frames):
+    """The oracle's rounded accumulators in units (second moments of ref and
+    dis, psnr noise) of the given frames, one frame per thread."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    def one(f):
+        s = oracle.moment_sums(ref[f], dis[f], bpc)
+        return (s[2], s[3]), oracle.psnr_noise_sum(ref[f], dis[f], bpc)
+
+    with ThreadPoolExecutor(max_workers=min(len(frames), os.cpu_count() or 1)) as ex:
+        res = list(ex.map(one, frames))
+    return (np.array([r[0] for r in res], dtype=np.uint64),
+            np.array([r[1] for r in res], dtype=np.uint64))
+
+
+def timed_outputs_exact(outs, want, s2_want, noise_want) -> bool:
+    """Every output of the timed calls equal, bit for bit, to the oracle's:
+    the last call's moments, MSE, psnr row sums and accumulators against the
+    oracle, and every other call's outputs against the last call's."""
+    import torch
+
+    def u64(t):
+        return t.cpu().view(torch.int64).numpy().view(np.uint64)
+
+    last = outs[-1]
+    n = want["moments"].shape[0]
+    ok = (np.array_equal(last["moments"].cpu().numpy()[:n].view(np.uint64),
+                         want["moments"].view(np.uint64)) and
+          np.array_equal(last["mse"].cpu().numpy()[:n].view(np.uint64), want["mse"].view(np.uint64)) and
+          np.array_equal(u64(last["psnr_rows"])[:n], want["psnr_rows"]) and
+          np.array_equal(u64(last["s2_sums"])[:n], s2_want) and
+          np.array_equal(u64(last["noise_sums"])[:n], noise_want))
+    def bits(t):
+        return t.view(torch.int64)  # doubles and uint64 compared as their bits
+
+    for o in outs[:-1]:
+        ok = ok and all(torch.equal(bits(o[k]), bits(last[k])) for k in last)
+    return bool(ok)
+
+
+def h2d_rate(pinned, dev, reps: int = 5) -> float:
+    """Page-locked host to device copy rate (GB/s) of one batch, best of reps."""
+    import torch
+    dst = torch.empty(pinned.shape, dtype=pinned.dtype, device=dev)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = 0.0
+    for _ in range(reps):
+        s.record()
+        dst.copy_(pinned, non_blocking=True)
+        e.record()
+        torch.cuda.synchronize()
+        best = max(best, pinned.numel() * pinned.element_size() / (s.elapsed_time(e) / 1e3) / 1e9)
+    return best
 
 
 def run_reference(args, rank, world, budget_s: float = 150.0):
@@ -259,43 +358,48 @@ def run_ours(args, rank, local_rank, world, pg):
     ref = torch.from_numpy(ref_h).to(dev)
     dis = torch.from_numpy(dis_h).to(dev)
     # The step: one fused call on the resident batch. Steps go in CUDA graphs
-    # of `depth` calls (api.FrameGraph; 16 when the step count allows), each
-    # kernel launched to overlap the one before it, as a stream of batches
-    # runs; every call does the whole work on its own workspace and outputs.
-    depth = next(d for d in (16, 8, 4, 2, 1) if args.steps % d == 0)
-    fg = api.FrameGraph(ref, dis, wl.bpc, features=3, depth=depth)
+    # of GRAPH_DEPTH calls (api.FrameGraph), each kernel launched to overlap
+    # the one before it, as a stream of batches runs, and a last, shorter
+    # graph for the steps that remain; every call does the whole work on its
+    # own workspace and outputs.
+    full, tail = divmod(args.steps, GRAPH_DEPTH)
+    graphs = []
+    if full:
+        graphs.append((api.FrameGraph(ref, dis, wl.bpc, features=3, depth=GRAPH_DEPTH, sums=True),
+                       full))
+    if tail:
+        graphs.append((api.FrameGraph(ref, dis, wl.bpc, features=3, depth=tail, sums=True), 1))
     stream = torch.cuda.current_stream(dev)
     kernels_per_step = 1
 
-    def replay():
-        return fg.replay()
-
     for _ in range(max(args.warmup, 3)):
-        replay()
+        for fg, _ in graphs:
+            fg.replay()
     torch.cuda.synchronize()
-    assert fg.status() == 0, "bounded device wait gave up"
+    assert all(fg.status() == 0 for fg, _ in graphs), "bounded device wait gave up"
 
-    replays = args.steps // depth
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(replays)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(replays)]
+    schedule = [fg for fg, n in graphs for _ in range(n)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in schedule]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in schedule]
 
     with Clocks(local_rank) as clocks:
         if pg is not None:
             dist.barrier(group=pg)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for i in range(replays):
+        for i, fg in enumerate(schedule):
             starts[i].record(stream)
-            replay()
+            fg.replay()
             ends[i].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         if pg is not None:
             dist.barrier(group=pg)
-    launches = kernels_per_step * args.steps  # graph replays: one kernel each
-    assert fg.status() == 0, "bounded device wait gave up"
-    per = [s.elapsed_time(e) / depth for s, e in zip(starts, ends)]  # ms per call
+    launches = kernels_per_step * args.steps  # graph replays: one kernel per call
+    assert all(fg.status() == 0 for fg, _ in graphs), "bounded device wait gave up"
+    last_outs = schedule[-1].outs  # the outputs of the last replay's calls
     device_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), pg)
+    per_call_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
     value = whole_job_rate(world, F, args.steps, device_ms / 1e3)
 
     # End to end through the host-memory entry point: pinned host frames in
@@ -314,34 +418,58 @@ def run_ours(args, rank, local_rank, world, pg):
                               ws=hws)
     e2e_s = max_over_ranks((time.perf_counter() - t1) / e2e_steps, pg)
     h2d, d2h = api.host_traffic(wl.width, wl.height, wl.width * 2, wl.bpc, F, 3)
+    link_gbs = h2d_rate(pin_r, dev)
     if rank != 0:
         return
 
     bytes_per_launch = F * wl.frame_pair_bytes
-    avg_ms = statistics.mean(per)
+    avg_ms = per_call_ms
     achieved = bytes_per_launch / (avg_ms / 1e3) / 1e9
     peak, peak_kind = peak_hbm()
+    e2e_value = whole_job_rate(world, F, 1, e2e_s)
     line = {
         "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": device_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u64", "data": "synthetic",
-        "config": dict(config(wl, F), parallelism=f"replicas x{world}"),
+        "config": dict(config(wl, F), parallelism=f"replicas x{world}",
+                       mode=f"stream of batches: CUDA graphs of {GRAPH_DEPTH} overlapping calls"
+                            + (f" (x{full})" if full else "")
+                            + (f", then one graph of {tail}" if tail else "")),
         "hbm_gbs": bytes_per_launch * args.steps / (device_ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(),
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "frac_nominal": achieved / NOMINAL_HBM_GBS,
+                     "peak_nominal": NOMINAL_HBM_GBS,
+                     "nominal_source": "nominal: GB300 HBM3e spec bandwidth",
                      "kernel": "frames_kernel (one launch per step)",
                      "algorithmic_bytes_per_launch": bytes_per_launch,
                      "avg_launch_ms": avg_ms},
-        "e2e": {"value": whole_job_rate(world, F, 1, e2e_s), "unit": "frames/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "frames/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "host_link_h2d_gbs": link_gbs,
+                "frac_of_host_link": e2e_value * wl.frame_pair_bytes / 1e9 / link_gbs,
+                "host_link_source": "page-locked host to device copy of the batch, best of 5, "
+                                    "same run"},
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),
         "wall_s": wall,
     }
-    line["cpu_baseline"] = cpu_baseline(ref_h, dis_h, wl.bpc, target_s=args.cpu_seconds)
+    base, want = cpu_baseline(ref_h, dis_h, wl.bpc, target_s=args.cpu_seconds)
+    line["cpu_baseline"] = base
+    n = want["moments"].shape[0]
+    s2_want, noise_want = oracle_accumulators(ref_h, dis_h, wl.bpc, list(range(n)))
+    exact = timed_outputs_exact(last_outs, want, s2_want, noise_want)
+    line["bit_exact"] = exact
+    line["frames_checked"] = n
+    line["bit_exact_note"] = (f"the last timed replay's {len(last_outs)} calls: every output of the "
+                              f"last call (moments, MSE, psnr row sums, second-moment and noise "
+                              f"accumulators) of frames 0..{n - 1} equal to the oracle's bit for "
+                              f"bit, and every call's outputs equal to the last call's")
     print(json.dumps(line), flush=True)
+    if not exact:
+        raise SystemExit("bench: the timed outputs differ from the oracle")
 
 
 def run_configs(args):

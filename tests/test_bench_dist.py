@@ -102,3 +102,69 @@ def test_reference_arm_prints_the_contract_line():
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert "workload" in d["config"]
+
+
+def test_profiled_traffic_reads_the_json_record(tmp_path, monkeypatch):
+    """roofline.traffic comes from the JSON record beside the ncu summary,
+    and only while its source hash matches the kernel code."""
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = tmp_path / "k.json"
+    monkeypatch.setattr(bench, "PROFILE", str(rec))
+    assert bench.profiled_traffic() is None  # no record
+    rec.write_text(json.dumps({"traffic_bytes_per_launch": 538512128,
+                               "kernel_sources_sha256_16": bench.kernel_hash()}))
+    assert bench.profiled_traffic() == 538512128
+    rec.write_text(json.dumps({"traffic_bytes_per_launch": 538512128,
+                               "kernel_sources_sha256_16": "0" * 16}))
+    assert bench.profiled_traffic() is None  # taken on other sources
+    rec.write_text("not json")
+    assert bench.profiled_traffic() is None
+
+
+def test_host_cpu_names_the_machine():
+    sys.path.insert(0, ROOT)
+    import platform
+
+    import bench
+    d = bench.host_cpu()
+    assert d["uname_m"] == platform.machine() and d["cpu_model"]
+
+
+def test_timed_outputs_check_catches_one_flipped_bit():
+    """The bench's exactness check compares the timed calls' outputs with the
+    oracle's bit for bit: a single changed bit in any output, or a call that
+    differs from the last, fails it (CPU tensors stand in for the device's)."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import torch
+
+    import bench
+    import oracle
+    from exact_reductions_gb300 import synth
+    wl = synth.WORKLOADS["T1"]
+    ref, dis = wl.batch(1)
+    ref, dis = ref[:, :64, :256].copy(), dis[:, :64, :256].copy()
+    want = oracle.batch(ref, dis, 16, threads=1)
+    s2, noise = bench.oracle_accumulators(ref, dis, 16, [0])
+
+    def as_u64(a):
+        return torch.from_numpy(np.array(a, copy=True).view(np.int64)).view(torch.uint64)
+
+    def outs():
+        return {"moments": torch.from_numpy(want["moments"].copy()),
+                "mse": torch.from_numpy(want["mse"].copy()),
+                "psnr_rows": as_u64(want["psnr_rows"]), "s2_sums": as_u64(s2),
+                "noise_sums": as_u64(noise)}
+
+    good = [outs(), outs()]
+    assert bench.timed_outputs_exact(good, want, s2, noise)
+    for key in ("moments", "mse", "psnr_rows", "s2_sums", "noise_sums"):
+        bad = [outs(), outs()]
+        v = bad[-1][key].view(torch.int64).view(-1)
+        v[0] ^= 1
+        assert not bench.timed_outputs_exact(bad, want, s2, noise), key
+        first = [outs(), outs()]
+        w = first[0][key].view(torch.int64).view(-1)
+        w[0] ^= 1
+        assert not bench.timed_outputs_exact(first, want, s2, noise), key
