@@ -100,7 +100,7 @@ bool make_layout(int width, int height, int bpc, int frames, int features, Layou
     L->blocks_per_frame = bpf;
     size_t off = 0;
     L->off_ctrl = off;
-    off = align256(off + (kCtrlWords + F * B + F * I) * sizeof(uint32_t));
+    off = align256(off + (kCtrlWords + F * B + (L->full ? F * I : 0)) * sizeof(uint32_t));
     L->ctrl_bytes = off;
     L->off_blocks = off;
     off = align256(off + F * B * sizeof(Agg));

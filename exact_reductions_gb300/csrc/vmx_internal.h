@@ -14,24 +14,28 @@ namespace vmx {
 #ifndef VMX_THREADS
 #define VMX_THREADS 128
 #endif
-// Threads per CTA: four independent warps; six CTAs per SM. Small CTAs free
-// their slots early when the items run out, for the next call's kernel.
+// Threads per CTA: four independent warps; six CTAs per SM (see
+// kMaxRegs). Small CTAs free their slots early when the items run out, for
+// the next call's kernel.
 constexpr int kThreads = VMX_THREADS;
 constexpr int kWarps = kThreads / 32;
-#ifndef VMX_MIN_BLOCKS
-#define VMX_MIN_BLOCKS 6
+#ifndef VMX_MAX_REGS
+#define VMX_MAX_REGS 80
 #endif
 #ifndef VMX_UNROLL
 #define VMX_UNROLL 3
 #endif
-constexpr int kMinBlocks = VMX_MIN_BLOCKS; // CTAs per SM the kernel is compiled for
+// Registers per thread of the frame kernel, at most: 80 keeps six CTAs of
+// 128 threads on an SM (registers go out 256 a warp). A cap, rather than
+// launch bounds asking for six CTAs, measured faster at the same count.
+constexpr int kMaxRegs = VMX_MAX_REGS;
 constexpr int kMaxRowsPerItem = 32;        // rows per item, at most
 #ifndef VMX_MAX_CHUNK
 #define VMX_MAX_CHUNK 4
 #endif
 constexpr int kMaxChunk = VMX_MAX_CHUNK;   // items a warp takes per ticket, at most
 #ifndef VMX_ITEM_PIXELS
-#define VMX_ITEM_PIXELS 4096
+#define VMX_ITEM_PIXELS 12288
 #endif
 constexpr int kItemPixels = VMX_ITEM_PIXELS; // target pixels per warp item
 #ifndef VMX_ITEM_PIXELS_FULL
@@ -62,24 +66,6 @@ constexpr uint32_t kPipeSpinLimit = 1u << 20;  // polls of one chunk's barrier, 
 #define VMX_FIRST_UNROLL 16
 #endif
 constexpr int kFirstUnroll = VMX_FIRST_UNROLL;  // loads in flight per lane in the walks' sequential sums
-#ifndef VMX_S1_MODE
-#define VMX_S1_MODE 0  // first moments: 0 dot products, 1 packed adds, 2 SIMD absolute-difference sums
-#endif
-#ifndef VMX_ODD_MODE
-#define VMX_ODD_MODE 0  // even-term marks: 0 dot products, 1 packed adds, 2 SIMD minimum sums
-#endif
-#ifndef VMX_LOOP_MODE
-#define VMX_LOOP_MODE 0  // 1: passes wholly inside a row in a loop of their own
-#endif
-#ifndef VMX_PREFETCH
-#define VMX_PREFETCH 0  // passes ahead that each warp starts into L2 (0: none)
-#endif
-#ifndef VMX_SMEM_ACC
-#define VMX_SMEM_ACC 0  // 1: flush-only row sums in shared memory, first moments summed per row
-#endif
-#ifndef VMX_FOLD_MODE
-#define VMX_FOLD_MODE 0  // block counts: 0 acquire-release, 1 relaxed, 2 relaxed and looked at an item later
-#endif
 #ifndef VMX_WHOLE_LOADS
 #define VMX_WHOLE_LOADS 1  // passes wholly inside a row load without per-vector checks
 #endif
@@ -102,7 +88,8 @@ enum Ctrl : int {
 // odd-term counts (ref in the low half of odd, dis in the high half). A
 // block's record is written by the block's last item to finish, from its
 // items' records. Whether a record is out is kept apart, in words cleared by
-// every call (an item's flag, a block's count of finished items).
+// every call (a block's count of finished items; an item's flag where the
+// look-back runs).
 struct alignas(16) Agg {
     uint64_t s2[2];
     uint64_t s1[2];
@@ -118,7 +105,7 @@ struct Layout {
     int rows_per_item, items_per_frame, blocks_per_frame;
     bool ordered;        // second moments may pass 2^53 units: odd counts per row
     bool full;           // ... and 2^55: look-back and row runs from binade 55 up
-    size_t off_ctrl;     // u32 [kCtrlWords] + finished items per block [F * B] + item flags [F * I]
+    size_t off_ctrl;     // u32 [kCtrlWords] + finished items per block [F * B] + item flags [F * I] (full)
     size_t ctrl_bytes;   // bytes cleared per call: the control words, counts and flags
     size_t off_blocks;   // Agg [F * B], written by each block's last item
     size_t off_items;    // Agg [F * I]
@@ -140,7 +127,8 @@ struct Params {
     int k;            // bpc - 8
     int rows_per_item, items_per_frame, blocks_per_frame;
     uint32_t *ctrl;
-    uint32_t *flags;      // per item: 0, 1 (its record is out), 2 (and its inclusive prefix)
+    uint32_t *flags;      // per item, frames that can pass 2^55 only: 0, 1 (its record is
+                          // out), 2 (and its inclusive prefix)
     uint32_t *block_fin;  // items of each block that have finished (32-bit counts)
     uint32_t *status;  // set to 1 when a bounded wait gives up
     Agg *items, *blocks;

@@ -51,12 +51,6 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void *ptr)
     return v;
 }
 
-// Starts a copy of `bytes` (a multiple of 16) from global memory into L2.
-__device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ uint32_t ld_u16(const unsigned char *ptr)
 {
     return __ldg(reinterpret_cast<const unsigned short *>(ptr));
@@ -84,13 +78,18 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *ptr, uint32_t v)
     return old;
 }
 
-// Adds v at GPU scope with no ordering of its own; returns the old value.
-__device__ __forceinline__ uint32_t atom_add_relaxed(uint32_t *ptr, uint32_t v)
+// Adds v at GPU scope with release order; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_release(uint32_t *ptr, uint32_t v)
 {
     uint32_t old;
-    asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
     return old;
 }
+
+// Orders the thread's earlier reads (a release RMW it observed) before its
+// later memory accesses, at GPU scope.
+__device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 
 
 // Sample type traits: a 16-byte vector holds 8 uint16 or 16 uint8 samples.
@@ -329,16 +328,14 @@ __device__ __forceinline__ Run warp_excl_run(const Run &x, int sh, Run *total)
 // A row's sums as the warp keeps them in shared memory for its item.
 struct alignas(8) RowSlot {
     uint64_t x, y, z, w;  // ref and dis second-moment sums, psnr sum, odd counts (ref | dis << 32)
-    uint64_t s1;          // the row's first-moment sums (ref | dis << 32), with VMX_SMEM_ACC
+    uint64_t s1;          // the row's first-moment sums (ref | dis << 32)
 };
 
 // A lane's row sums that only the flushes touch, in shared memory (one slot
 // per lane of each warp) so that they hold no registers across the passes.
 struct LaneRowAcc {
     uint64_t t2r[32], t2d[32], tp[32];
-    uint32_t even[32];
 };
-constexpr bool kSmemAcc = VMX_SMEM_ACC != 0;
 
 struct RowSums {
     uint64_t t2r, t2d, tp, s1r, s1d;
@@ -357,18 +354,21 @@ struct RowSums {
 // are integers of at most 2^7 and add exactly in binary32.
 // Odd terms: a binary32 square of a codeword is odd exactly when the codeword
 // is odd and below 4096, i.e. its bits 0 and 12-15 read 1 and 0; the even
-// terms are counted (a halfword minimum marks them, a dot product adds the
-// marks) and the row's end takes them from its number of samples.
-// First moments: the samples' sums by a dot product with (1, 1).
-// Each flush folds its rounding errors into the row's term sums at once.
+// terms are counted (a halfword minimum marks them, 0 or 1 in each
+// halfword, and the marks are added as packed halfword counts) and the row's
+// end takes them from its number of samples.
+// First moments: two packed adds a word (the word itself and its high
+// sample). The dot products run on the FMA-heavy pipe, as do the packed
+// binary32 operations; the adds run on the integer ALU, which has room.
+// Each flush folds its rounding errors into the row's term sums (kept in
+// shared memory) at once.
 struct Acc16 {
     uint32_t lr, hr, ld, hd, lx, hx;  // dot-product sums since the last flush
-    uint32_t nzr, nzd;                // samples with even terms since the last flush
+    uint32_t nzr, nzd;                // the row's even terms so far (two halfword counts each)
     float2 er, ed, ep;                // rounding errors since the last flush
-    uint32_t s1r, s1d;                // row sums of the samples (first moments)
-    uint32_t s1rh, s1dh;              // row sums of the words' high samples (packed first moments)
-    uint32_t even;                    // row's even terms (ref low half, dis high)
-    uint64_t t2r, t2d, tp;            // row sums of the terms: squares of p, of q, of d
+    uint32_t s1r, s1d;                // row sums of the words (first moments, packed)
+    uint32_t s1rh, s1dh;              // row sums of the words' high samples
+    uint64_t tp;                      // psnr alone: the row's sum of the terms
 };
 
 __device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
@@ -376,69 +376,21 @@ __device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y
 // Each unsigned halfword of x, or 1 if that is smaller.
 __device__ __forceinline__ uint32_t halfword_min1(uint32_t x) { return __vminu2(x, 0x00010001u); }
 
-// c plus the sum of the absolute differences of the halfwords of a and b.
-__device__ __forceinline__ uint32_t vsad2_add(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("vabsdiff2.u32.u32.u32.add %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
-// c plus the sum of the unsigned halfword minima of a and b.
-__device__ __forceinline__ uint32_t vmin2_add(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("vmin2.u32.u32.u32.add %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
-// First moments of a word of two 16-bit samples into the lane's row sums.
+// First moments of a word of two 16-bit samples into the lane's row sums by
+// two adds: the word itself (p0 + 2^16 p1, modulo 2^32) and its high sample.
 __device__ __forceinline__ void acc16_s1(uint32_t &s, uint32_t &sh, uint32_t w)
 {
-#if VMX_S1_MODE == 0
-    s = __dp2a_lo(w, 0x00000101u, s);  // p0 + p1
-    (void)sh;
-#elif VMX_S1_MODE == 1
-    s += w;         // p0 + 2^16 p1, modulo 2^32
-    sh += w >> 16;  // p1
-#else
-    s = vsad2_add(w, 0u, s);
-    (void)sh;
-#endif
+    s += w;
+    sh += w >> 16;
 }
 
-// The row's first-moment sum of a lane from its accumulators.
-__device__ __forceinline__ uint32_t s1_total(uint32_t s, uint32_t sh)
-{
-#if VMX_S1_MODE == 1
-    return (s - (sh << 16)) + sh;  // the low samples' sum is below 2^32
-#else
-    (void)sh;
-    return s;
-#endif
-}
+// The lane's first-moment sum of a row from its two sums (the low samples'
+// sum, s - 2^16 sh modulo 2^32, is below 2^32).
+__device__ __forceinline__ uint32_t s1_total(uint32_t s, uint32_t sh) { return (s - (sh << 16)) + sh; }
 
-// Even-term marks (halfwords of 0 or 1) into the lane's count.
-__device__ __forceinline__ void acc16_even(uint32_t &n, uint32_t marks)
-{
-#if VMX_ODD_MODE == 0
-    n = __dp2a_lo(marks, 0x00000101u, n);
-#elif VMX_ODD_MODE == 1
-    n += marks;  // two halfword counts, each at most 512 a row
-#else
-    n = vsad2_add(marks, 0u, n);
-#endif
-}
-
-// The lane's count of even terms of a row from its accumulator.
-__device__ __forceinline__ uint32_t even_total(uint32_t n)
-{
-#if VMX_ODD_MODE == 1
-    return (n & 0xffffu) + (n >> 16);
-#else
-    return n;
-#endif
-}
+// The lane's count of even terms of a row from its halfword counts (marks of
+// 0 or 1 added as two halfwords, each at most 512 a row).
+__device__ __forceinline__ uint32_t even_total(uint32_t n) { return (n & 0xffffu) + (n >> 16); }
 
 template <bool M, bool P, bool ODD>
 __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
@@ -466,13 +418,8 @@ __device__ __forceinline__ void acc16_word(Acc16 &a, uint32_t r, uint32_t d)
             // Per 16-bit sample: zero exactly when it is odd and below 4096;
             // the unsigned halfword minimum with 1 marks the others.
             const uint32_t tr = (r & 0xF001F001u) ^ 0x00010001u, td = (d & 0xF001F001u) ^ 0x00010001u;
-#if VMX_ODD_MODE == 2
-            a.nzr = vmin2_add(tr, 0x00010001u, a.nzr);
-            a.nzd = vmin2_add(td, 0x00010001u, a.nzd);
-#else
-            acc16_even(a.nzr, halfword_min1(tr));
-            acc16_even(a.nzd, halfword_min1(td));
-#endif
+            a.nzr += halfword_min1(tr);
+            a.nzd += halfword_min1(td);
         }
     }
     if (P) {
@@ -506,8 +453,8 @@ __device__ __forceinline__ void acc16_word_low(Acc16 &a, uint32_t r, uint32_t d)
         acc16_s1(a.s1r, a.s1rh, r);
         acc16_s1(a.s1d, a.s1dh, d);
         if (ODD) {
-            acc16_even(a.nzr, ~r & 0x00010001u);
-            acc16_even(a.nzd, ~d & 0x00010001u);
+            a.nzr += ~r & 0x00010001u;
+            a.nzd += ~d & 0x00010001u;
         }
     } else if (P) {
         const int32_t i0 = (int32_t)(r & 0xffffu) - (int32_t)(d & 0xffffu);
@@ -527,42 +474,20 @@ __device__ __forceinline__ void acc16_flush(Acc16 &a, LaneRowAcc &sa, int lane)
     if (M) {
         const uint64_t pr = ((uint64_t)a.hr << 8) + a.lr;  // sums of p^2, q^2
         const uint64_t pd = ((uint64_t)a.hd << 8) + a.ld;
-        const uint64_t xr = pr - (uint64_t)(int64_t)small_f_to_i(__fadd_rn(a.er.x, a.er.y));
-        const uint64_t xd = pd - (uint64_t)(int64_t)small_f_to_i(__fadd_rn(a.ed.x, a.ed.y));
-        if (kSmemAcc) {
-            sa.t2r[lane] += xr;
-            sa.t2d[lane] += xd;
-        } else {
-            a.t2r += xr;
-            a.t2d += xd;
-        }
+        sa.t2r[lane] += pr - (uint64_t)(int64_t)small_f_to_i(__fadd_rn(a.er.x, a.er.y));
+        sa.t2d[lane] += pd - (uint64_t)(int64_t)small_f_to_i(__fadd_rn(a.ed.x, a.ed.y));
         if (P) {
             const uint64_t px = ((uint64_t)a.hx << 8) + a.lx;  // sum of p q
-            const uint64_t xp = pr + pd - 2ull * px - (uint64_t)ep;
-            if (kSmemAcc) sa.tp[lane] += xp;
-            else a.tp += xp;
+            sa.tp[lane] += pr + pd - 2ull * px - (uint64_t)ep;
             a.lx = a.hx = 0;
         }
         a.lr = a.hr = a.ld = a.hd = 0;
         a.er = a.ed = make_float2(0.0f, 0.0f);
-        if (ODD && VMX_ODD_MODE == 0) {
-            if (kSmemAcc) sa.even[lane] += a.nzr | (a.nzd << 16);
-            else a.even += a.nzr | (a.nzd << 16);
-            a.nzr = a.nzd = 0;
-        }
     } else if (P) {
         a.tp -= (uint64_t)ep;
     }
     if (P) a.ep = make_float2(0.0f, 0.0f);
 }
-
-// The first pass of the next row of an item, loaded during the current
-// row's last pass (rotating loads across the rows of an item).
-struct RowPrefetch {
-    uint4 R[kUnroll], D[kUnroll];
-    bool have;                     // R, D hold this row's first pass
-    const unsigned char *nr, *nd;  // the item's next row, or null
-};
 
 // With STG the row's whole chunks come through the warp's chunk stream (the
 // row is the stream's next `cpr` chunks), the rest of the row straight from
@@ -572,7 +497,7 @@ struct RowPrefetch {
 // depth) the full one.
 template <bool M, bool P, bool ODD, bool VEC, bool STG, bool LOW>
 __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, int width, Pipe &pp,
-                              const PipeSrc &src, uint32_t *status, RowPrefetch &pf)
+                              const PipeSrc &src, uint32_t *status)
 {
     static_assert(kUnroll * 8 <= kFlushSamples, "an iteration holds at most kFlushSamples per lane");
     static_assert(kFlushSamples <= 256, "dot-product sums must stay below 2^32");
@@ -580,10 +505,7 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
     Acc16 a = {};
     __shared__ LaneRowAcc lane_acc[kWarps];
     LaneRowAcc &sa = lane_acc[threadIdx.x >> 5];
-    if (kSmemAcc && M) {
-        sa.t2r[lane] = sa.t2d[lane] = sa.tp[lane] = 0;
-        sa.even[lane] = 0;
-    }
+    if (M) sa.t2r[lane] = sa.t2d[lane] = sa.tp[lane] = 0;
     const int nvt = (width + 7) >> 3;
     // Vectors wholly inside the row (all of them but a ragged last one).
     const int nfull = width >> 3;
@@ -613,132 +535,6 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
             pend += 8 * kUnroll;
         }
     }
-#if VMX_LOOP_MODE >= 2
-    if (VEC && !STG) {
-        // Whole passes with rotating loads: vector u of the next pass is
-        // loaded as soon as vector u of this pass has been used.
-        const int npass = nfull / (32 * kUnroll);
-        const bool whole_row = nfull == nvt && npass * 32 * kUnroll == nfull;
-        if (npass > 0) {
-            const uint4 *vr = reinterpret_cast<const uint4 *>(rr) + lane;
-            const uint4 *vd = reinterpret_cast<const uint4 *>(dr) + lane;
-            uint4 R[kUnroll], D[kUnroll];
-            if (VMX_LOOP_MODE == 3 && pf.have) {
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    R[u] = pf.R[u];
-                    D[u] = pf.D[u];
-                }
-            } else {
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    R[u] = ld_nc_v4(vr + 32 * u);
-                    D[u] = ld_nc_v4(vd + 32 * u);
-                }
-            }
-            bool pre = false;
-            for (int ps = 0; ps < npass; ++ps) {
-                if (pend + 8 * kUnroll > kFlushSamples) {
-                    acc16_flush<M, P, ODD>(a, sa, lane);
-                    pend = 0;
-                }
-                bool low = false;
-                if (LOW) {
-                    uint32_t o = 0;
-#pragma unroll
-                    for (int u = 0; u < kUnroll; ++u)
-                        o |= R[u].x | R[u].y | R[u].z | R[u].w | D[u].x | D[u].y | D[u].z | D[u].w;
-                    low = !__any_sync(kFull, (o & 0xF000F000u) != 0u);
-                }
-                const bool more = ps + 1 < npass;
-                const bool next_row = VMX_LOOP_MODE == 3 && !more && whole_row && pf.nr != nullptr;
-                pre = more || next_row;
-                const uint4 *nr = more ? vr + 32 * kUnroll
-                                       : (next_row ? reinterpret_cast<const uint4 *>(pf.nr) + lane : vr);
-                const uint4 *nd = more ? vd + 32 * kUnroll
-                                       : (next_row ? reinterpret_cast<const uint4 *>(pf.nd) + lane : vd);
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const uint4 r = R[u], d = D[u];
-                    if (LOW && low) {
-                        acc16_word_low<M, P, ODD>(a, r.x, d.x);
-                        acc16_word_low<M, P, ODD>(a, r.y, d.y);
-                        acc16_word_low<M, P, ODD>(a, r.z, d.z);
-                        acc16_word_low<M, P, ODD>(a, r.w, d.w);
-                    } else {
-                        acc16_word<M, P, ODD>(a, r.x, d.x);
-                        acc16_word<M, P, ODD>(a, r.y, d.y);
-                        acc16_word<M, P, ODD>(a, r.z, d.z);
-                        acc16_word<M, P, ODD>(a, r.w, d.w);
-                    }
-                    if (pre) {
-                        R[u] = ld_nc_v4(nr + 32 * u);
-                        D[u] = ld_nc_v4(nd + 32 * u);
-                    }
-                }
-                vr = nr;
-                vd = nd;
-                pend += 8 * kUnroll;
-            }
-            base = npass * 32 * kUnroll;
-            if (VMX_LOOP_MODE == 3) {
-                pf.have = pre;
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    pf.R[u] = R[u];
-                    pf.D[u] = D[u];
-                }
-            }
-        }
-    }
-#endif
-#if VMX_LOOP_MODE == 1
-    if (VEC && !STG) {
-        // Passes wholly inside the row: every load and word unconditional.
-        const uint4 *vr = reinterpret_cast<const uint4 *>(rr) + lane;
-        const uint4 *vd = reinterpret_cast<const uint4 *>(dr) + lane;
-        for (; base + 32 * kUnroll <= nfull; base += 32 * kUnroll) {
-            if (pend + 8 * kUnroll > kFlushSamples) {
-                acc16_flush<M, P, ODD>(a, sa, lane);
-                pend = 0;
-            }
-            uint4 R[kUnroll], D[kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                R[u] = ld_nc_v4(vr + 32 * u);
-                D[u] = ld_nc_v4(vd + 32 * u);
-            }
-            vr += 32 * kUnroll;
-            vd += 32 * kUnroll;
-            bool low = false;
-            if (LOW) {
-                uint32_t o = 0;
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u)
-                    o |= R[u].x | R[u].y | R[u].z | R[u].w | D[u].x | D[u].y | D[u].z | D[u].w;
-                low = !__any_sync(kFull, (o & 0xF000F000u) != 0u);
-            }
-            if (LOW && low) {
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    acc16_word_low<M, P, ODD>(a, R[u].x, D[u].x);
-                    acc16_word_low<M, P, ODD>(a, R[u].y, D[u].y);
-                    acc16_word_low<M, P, ODD>(a, R[u].z, D[u].z);
-                    acc16_word_low<M, P, ODD>(a, R[u].w, D[u].w);
-                }
-            } else {
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    acc16_word<M, P, ODD>(a, R[u].x, D[u].x);
-                    acc16_word<M, P, ODD>(a, R[u].y, D[u].y);
-                    acc16_word<M, P, ODD>(a, R[u].z, D[u].z);
-                    acc16_word<M, P, ODD>(a, R[u].w, D[u].w);
-                }
-            }
-            pend += 8 * kUnroll;
-        }
-    }
-#endif
     for (; base < nvt; base += 32 * kUnroll) {
         // Vectors per lane this time (the same for the whole warp): kUnroll
         // but at the row's end, where vectors past it are skipped.
@@ -752,18 +548,6 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
         // Every vector of this iteration inside the row (the warp agrees):
         // plain 16-byte loads without per-vector checks.
         if (VEC && base + 32 * kUnroll <= nfull) {
-#if VMX_PREFETCH > 0
-            // Lanes 0 and 1 start the pass VMX_PREFETCH passes ahead (this
-            // row's, else the item's next row's) on its way into L2.
-            if (lane < 2) {
-                const int t = base + VMX_PREFETCH * 32 * kUnroll;
-                const unsigned char *row = lane ? dr : rr;
-                const unsigned char *nxt = lane ? pf.nd : pf.nr;
-                if (t + 32 * kUnroll <= nfull) prefetch_l2(row + 16 * (size_t)t, 512u * kUnroll);
-                else if (nxt && t >= nvt && t - nvt + 32 * kUnroll <= nfull)
-                    prefetch_l2(nxt + 16 * (size_t)(t - nvt), 512u * kUnroll);
-            }
-#endif
             const uint4 *vr = reinterpret_cast<const uint4 *>(rr) + base + lane;
             const uint4 *vd = reinterpret_cast<const uint4 *>(dr) + base + lane;
 #pragma unroll
@@ -817,21 +601,17 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
     acc16_flush<M, P, ODD>(a, sa, lane);
     RowSums out = {0, 0, 0, 0, 0, 0, 0};
     if (M) {
-        out.t2r = kSmemAcc ? sa.t2r[lane] : a.t2r;
-        out.t2d = kSmemAcc ? sa.t2d[lane] : a.t2d;
-        out.s1r = s1_total(a.s1r, a.s1rh);
-        out.s1d = s1_total(a.s1d, a.s1dh);
-        if (kSmemAcc) {  // row totals (a lane's share is below 2^26, the row's below 2^31)
-            out.s1r = warp_sum32((uint32_t)out.s1r);
-            out.s1d = warp_sum32((uint32_t)out.s1d);
-        }
+        out.t2r = sa.t2r[lane];
+        out.t2d = sa.t2d[lane];
+        // Row totals of the first moments (a lane's share is below 2^26,
+        // the row's below 2^31).
+        out.s1r = warp_sum32(s1_total(a.s1r, a.s1rh));
+        out.s1d = warp_sum32(s1_total(a.s1d, a.s1dh));
     }
-    uint32_t even = kSmemAcc && M ? sa.even[lane] : a.even;
-    if (ODD && VMX_ODD_MODE != 0) even = even_total(a.nzr) | (even_total(a.nzd) << 16);
-    if (P) out.tp = kSmemAcc && M ? sa.tp[lane] : a.tp;
-    // Row totals; without VMX_SMEM_ACC the first-moment sums stay per lane
-    // (the item adds them).
-    // (a lane's sums of a row stay below 2^42: at most 1024 terms below 2^32)
+    const uint32_t even = ODD ? even_total(a.nzr) | (even_total(a.nzd) << 16) : 0u;
+    if (P) out.tp = M ? sa.tp[lane] : a.tp;
+    // Row totals (a lane's sums of a row stay below 2^42: at most 1024 terms
+    // below 2^32).
     out.t2r = warp_sum_lt51(out.t2r);
     out.t2d = warp_sum_lt51(out.t2d);
     out.tp = warp_sum_lt51(out.tp);
@@ -880,8 +660,8 @@ __device__ RowSums row_sums8(const unsigned char *rr, const unsigned char *dr, i
     out.t2r = warp_sum32(s2r);
     out.t2d = warp_sum32(s2d);
     out.tp = P ? out.t2r + out.t2d - 2ull * warp_sum32(srd) : 0ull;
-    out.s1r = kSmemAcc ? warp_sum32(s1r) : s1r;  // per lane without VMX_SMEM_ACC (the item adds them)
-    out.s1d = kSmemAcc ? warp_sum32(s1d) : s1d;
+    out.s1r = M ? warp_sum32(s1r) : 0;  // row totals (below 2^23)
+    out.s1d = M ? warp_sum32(s1d) : 0;
     out.oddr = out.oddd = 0;
     return out;
 }
@@ -1283,11 +1063,12 @@ __device__ __forceinline__ bool item_done(const Params &p, int f, int i)
     return ld_acquire(p.flags + (size_t)f * p.items_per_frame + i) != 0u;
 }
 
-// Called by the whole warp of block b's last item to finish: each lane reads
-// one item's record (after an acquire of its flag), the warp adds them, and
-// lane 0 writes the block's record and then, with release order, sets the
-// block's count one past its items. Item sums stay below 2^48 (at most 2^16
-// pixels of terms below 2^32).
+// Called by the whole warp of block b's last item to finish, after lane 0
+// has acquired the block's count (every item released its record before it
+// counted itself): each lane reads one item's record, the warp adds them,
+// and lane 0 writes the block's record and then, with release order, sets
+// the block's count one past its items. Item sums stay below 2^48 (at most
+// 2^16 pixels of terms below 2^32).
 __device__ __noinline__ void fold_block(const Params &p, int f, int b)
 {
     const int lane = lane_id(), I = p.items_per_frame;
@@ -1295,17 +1076,6 @@ __device__ __noinline__ void fold_block(const Params &p, int f, int b)
     Agg g = agg_zero();
     if (lane < (int)block_items(p, b)) {
         const Agg *it = p.items + (size_t)f * I + i;
-        // Every item of the block has counted itself, each after releasing
-        // its flag; with a relaxed count the flag may still be on its way,
-        // so wait for it (bounded).
-        uint32_t spins = 0;
-        while (!item_done(p, f, i)) {
-            if (VMX_FOLD_MODE == 0 || ++spins > p.spin_limit) {
-                if (VMX_FOLD_MODE != 0) atomicOr(p.status, 1u);
-                break;
-            }
-            __nanosleep(32);
-        }
         g.s2[0] = __ldcg(&it->s2[0]);
         g.s2[1] = __ldcg(&it->s2[1]);
         g.s1[0] = __ldcg(&it->s1[0]);
@@ -1394,6 +1164,7 @@ __device__ WindowScan scan_window(bool done, SC v, SC run)
 // looks at the 32 blocks from the first incomplete one), the first
 // incomplete block item by item: an item is complete once its flag is set. A wait on one block is bounded. *before gets the prefix
 // (sum, odd terms) before the item returned.
+template <bool FLAGS>
 __device__ int crossing_item(const Params &p, int f, int X, SC *before)
 {
     const int lane = lane_id(), NB = p.blocks_per_frame, I = p.items_per_frame;
@@ -1425,6 +1196,15 @@ __device__ int crossing_item(const Params &p, int f, int X, SC *before)
         run = sc_add(run, w.tot);
         base += w.first_open;
         if (w.first_open > 0) continue;
+        if (!FLAGS) {  // items keep no flags of their own: wait for the block
+            if (++spins > p.spin_limit) {
+                if (lane == 0) atomicOr(p.status, 1u);
+                *before = run;
+                return I;
+            }
+            __nanosleep(64);
+            continue;
+        }
         // Block `base` is incomplete: poll its items alone until the
         // crossing shows among its complete ones or all of them are out.
         const int i = base * kBlockItems + lane;
@@ -1619,7 +1399,7 @@ __device__ uint64_t walk_plane_fast(const Params &p, int f, int X, Agg *t)
     const uint64_t *R = p.s2_rows + off;
     const uint32_t *O = p.odd_rows + off;
     SC pre_items;
-    const int it = crossing_item(p, f, X, &pre_items);
+    const int it = crossing_item<FULL>(p, f, X, &pre_items);
     if (it >= I) {
         *t = frame_totals(p, f, X);
         count(p.ctrl, kCtrlRowsExact, (uint32_t)H);
@@ -1771,7 +1551,7 @@ __device__ __forceinline__ void item_of_ticket(int tk, int F, int I, int *f, int
 }
 
 template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC, bool LOW>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
+__global__ void __maxnreg__(kMaxRegs) frames_kernel(Params p)
 {
     const int lane = lane_id();
     const int I = p.items_per_frame, NB = p.blocks_per_frame;
@@ -1808,10 +1588,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t nwarps = gridDim.x * (uint32_t)kWarps;
     uint32_t cur = 0u, end = 0u, seen = 0u;
-#if VMX_FOLD_MODE == 2
-    uint32_t fold_old = 0u, fold_n = 0u;  // the previous item's count (lane 0) and its block's size
-    int fold_f = -1, fold_b = 0;
-#endif
     for (;;) {
         if (cur >= end) {
             const uint32_t left = (uint32_t)nitems > seen ? (uint32_t)nitems - seen : 0u;
@@ -1841,16 +1617,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         // A. exact row sums. Lane 0 records each row and keeps its sums in
         // the warp's shared slots, so that no item totals stay live in
         // registers across rows; lane i reads row i's back afterwards.
-        uint32_t s1r = 0, s1d = 0;  // this lane's first-moment sums
-        RowPrefetch pf;
-        pf.have = false;
         for (int r = r0; r < r1; ++r) {
             const unsigned char *rr = fr + (int64_t)r * p.stride;
             const unsigned char *dr = fd + (int64_t)r * p.stride;
-            pf.nr = r + 1 < r1 ? rr + p.stride : nullptr;
-            pf.nd = r + 1 < r1 ? dr + p.stride : nullptr;
             const RowSums rs = sizeof(TS) == 2
-                                   ? row_sums16<M, P, ODD, VEC, STG, LOW>(rr, dr, p.width, pp, src, p.status, pf)
+                                   ? row_sums16<M, P, ODD, VEC, STG, LOW>(rr, dr, p.width, pp, src, p.status)
                                    : row_sums8<M, P, VEC>(rr, dr, p.width);
             if (lane == 0) {
                 if (M) {
@@ -1863,31 +1634,25 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
                 }
                 if (P) p.psnr_rows[(size_t)f * H + r] = rs.tp;
             }
-            if (!kSmemAcc) {
-                s1r += (uint32_t)rs.s1r;
-                s1d += (uint32_t)rs.s1d;
-            }
             if (lane == 0)
                 item_rows[wid][r - r0] = RowSlot{rs.t2r, rs.t2d, rs.tp, (uint64_t)rs.oddr | ((uint64_t)rs.oddd << 32),
                                                  rs.s1r | (rs.s1d << 32)};
         }
         __syncwarp();
         uint64_t my_r = 0, my_d = 0, my_p = 0, my_o = 0;  // this lane's row of the item
+        uint32_t s1r = 0, s1d = 0;
         if (lane < r1 - r0) {
             const RowSlot v = item_rows[wid][lane];
             my_r = v.x;
             my_d = v.y;
             my_p = v.z;
             my_o = v.w;
-            if (kSmemAcc) {
-                s1r = (uint32_t)v.s1;
-                s1d = (uint32_t)(v.s1 >> 32);
-            }
+            s1r = (uint32_t)v.s1;
+            s1d = (uint32_t)(v.s1 >> 32);
         }
         __syncwarp();
         // Lane 0 alone stores and adds the item's sums: a one-row item has
-        // them in lane 0 already. A lane's first-moment sum of an item fits
-        // 32 bits (at most 32 rows of 1024 samples below 2^16 a lane).
+        // them in lane 0 already. A row's first-moment sum is below 2^31.
         Agg g = agg_zero();
         const bool one = r1 - r0 == 1;
         if (M) {
@@ -1905,7 +1670,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         if (lane == 0) {
             Agg *ia = p.items + (size_t)f * I + j;
             store_agg(ia, g);
-            st_release(p.flags + (size_t)f * I + j, 1u);  // the item's sums are out
+            // The look-back reads each item's flag: its sums are out.
+            if (FULL) st_release(p.flags + (size_t)f * I + j, 1u);
         }
 
         // B. frames that can pass 2^55: runs of the rows planned from 55 up.
@@ -1940,38 +1706,23 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) frames_kernel(Params p)
         // block's last item to finish writes the block's record. (A test of
         // the bounded waits asks for one item more than a block holds: no
         // block completes.)
-#if VMX_FOLD_MODE == 2
-        // The count is relaxed and its old value is looked at one item
-        // later (or when the warp runs out of items), so that no warp waits
-        // for it.
-        if (fold_f >= 0 && __shfl_sync(kFull, fold_old, 0) + 1u == fold_n) fold_block(p, fold_f, fold_b);
         {
-            const int b = j / kBlockItems;
-            if (lane == 0) fold_old = atom_add_relaxed(p.block_fin + (size_t)f * NB + b, 1u);
-            fold_f = f;
-            fold_b = b;
-            fold_n = block_items(p, b) + p.test_stall;
-        }
-#else
-        {
+            // One release per item (its records, then its count); the last
+            // item of the block acquires them all with one fence.
             const int b = j / kBlockItems;
             uint32_t last = 0;
             if (lane == 0) {
-                const uint32_t old = VMX_FOLD_MODE == 0
-                                         ? atom_add_acq_rel(p.block_fin + (size_t)f * NB + b, 1u)
-                                         : atom_add_relaxed(p.block_fin + (size_t)f * NB + b, 1u);
+                uint32_t *cnt = p.block_fin + (size_t)f * NB + b;
+                const uint32_t old = FULL ? atom_add_acq_rel(cnt, 1u) : atom_add_release(cnt, 1u);
                 last = old + 1u == block_items(p, b) + p.test_stall ? 1u : 0u;
+                if (last && !FULL) fence_acq_rel();
             }
             if (__shfl_sync(kFull, last, 0)) {
                 __syncwarp();  // lane 0's acquire before the other lanes' reads
                 fold_block(p, f, b);
             }
         }
-#endif
     }
-#if VMX_FOLD_MODE == 2
-    if (fold_f >= 0 && __shfl_sync(kFull, fold_old, 0) + 1u == fold_n) fold_block(p, fold_f, fold_b);
-#endif
 
     // Every chunk a warp started it has read, unless a wait gave up: then
     // wait (bounded) for the copies still landing in its buffers.

@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module")
 def staged():
-    return _lib.bind(build.build_variant("staged3", ["VMX_STAGES=3", "VMX_MIN_BLOCKS=4"]))
+    return _lib.bind(build.build_variant("staged3", ["VMX_STAGES=3", "VMX_MAX_REGS=128"]))
 
 
 def test_staged_rows_match_oracle(monkeypatch, staged):

@@ -20,11 +20,12 @@ def test_noalloc_rejects_without_touching_the_device():
     """Shape errors come back before any CUDA call (runs without a GPU)."""
     lib = _lib.load()
     fake = ctypes.c_void_p(256)
-    # 16-bit 3840x2160 needs about 7.5 MiB of scratch per 64 frames.
-    need = lib.vmx_workspace_bytes(3840, 2160, 16, 160, 3)
+    # A batch of 16-bit 3840x2160 frames too large for the fixed scratch.
+    big = 1024
+    need = lib.vmx_workspace_bytes(3840, 2160, 16, big, 3)
     assert need > _lib.NOALLOC_SCRATCH_BYTES
     before = lib.vmx_kernel_launches()
-    rc = lib.vmx_frames_noalloc(fake, fake, 3840, 2160, 7680, 16, 160, 3, fake, None, None,
+    rc = lib.vmx_frames_noalloc(fake, fake, 3840, 2160, 7680, 16, big, 3, fake, None, None,
                                 fake, fake, None, None, None)
     assert rc == _lib.VMX_ESCRATCH
     assert b"scratch" in lib.vmx_strerror(rc)
