@@ -37,7 +37,18 @@ METRIC = "frames/s and achieved HBM GB/s (fraction of peak), 16-bit 3840x2160, b
 WORKLOAD = "C4"
 PROFILE = os.path.join(ROOT, "profiles", "frames_kernel_c4.json")
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, the vendor's figure (context only)
-GRAPH_DEPTH = 16          # calls per graph replay in the timed stream of batches
+GRAPH_DEPTH = 16          # calls per graph replay in the timed stream of batches, at least
+
+
+def graph_plan(steps: int):
+    """Depths of the graphs that K steps run as: as many graphs as hold at
+    least GRAPH_DEPTH calls each, the steps shared out evenly (so every graph
+    holds 16 to 31 calls once K >= 16), or one graph of K calls below that."""
+    if steps < GRAPH_DEPTH:
+        return [steps]
+    n = steps // GRAPH_DEPTH
+    base, extra = divmod(steps, n)
+    return [base + 1] * extra + [base] * (n - extra)
 KERNEL_SOURCES = [os.path.join(ROOT, "exact_reductions_gb300", "csrc", f)
                   for f in ("vmx_kernels.cu", "ordsum.cuh", "vmx_internal.h")]
 
@@ -358,17 +369,13 @@ def run_ours(args, rank, local_rank, world, pg):
     ref = torch.from_numpy(ref_h).to(dev)
     dis = torch.from_numpy(dis_h).to(dev)
     # The step: one fused call on the resident batch. Steps go in CUDA graphs
-    # of GRAPH_DEPTH calls (api.FrameGraph), each kernel launched to overlap
-    # the one before it, as a stream of batches runs, and a last, shorter
-    # graph for the steps that remain; every call does the whole work on its
-    # own workspace and outputs.
-    full, tail = divmod(args.steps, GRAPH_DEPTH)
-    graphs = []
-    if full:
-        graphs.append((api.FrameGraph(ref, dis, wl.bpc, features=3, depth=GRAPH_DEPTH, sums=True),
-                       full))
-    if tail:
-        graphs.append((api.FrameGraph(ref, dis, wl.bpc, features=3, depth=tail, sums=True), 1))
+    # of 16 to 31 calls each (api.FrameGraph; graph_plan), each kernel
+    # launched to overlap the one before it, as a stream of batches runs;
+    # every call does the whole work on its own workspace and outputs.
+    plan = graph_plan(args.steps)
+    depths = sorted(set(plan), reverse=True)
+    made = {d: api.FrameGraph(ref, dis, wl.bpc, features=3, depth=d, sums=True) for d in depths}
+    graphs = [(made[d], plan.count(d)) for d in depths]
     stream = torch.cuda.current_stream(dev)
     kernels_per_step = 1
 
@@ -433,9 +440,8 @@ def run_ours(args, rank, local_rank, world, pg):
         "ms_per_step": device_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u64", "data": "synthetic",
         "config": dict(config(wl, F), parallelism=f"replicas x{world}",
-                       mode=f"stream of batches: CUDA graphs of {GRAPH_DEPTH} overlapping calls"
-                            + (f" (x{full})" if full else "")
-                            + (f", then one graph of {tail}" if tail else "")),
+                       mode="stream of batches: " + ", ".join(
+                           f"{plan.count(d)} CUDA graph(s) of {d} overlapping calls" for d in depths)),
         "hbm_gbs": bytes_per_launch * args.steps / (device_ms / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(),

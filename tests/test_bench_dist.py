@@ -168,3 +168,20 @@ def test_timed_outputs_check_catches_one_flipped_bit():
         w = first[0][key].view(torch.int64).view(-1)
         w[0] ^= 1
         assert not bench.timed_outputs_exact(first, want, s2, noise), key
+
+
+def test_graph_plan_keeps_every_graph_at_least_sixteen_deep():
+    """Every step count of 16 or more runs as graphs of 16 to 31 calls (the
+    same mode for the driver's 20 steps and a long run); fewer steps run as
+    one graph."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.graph_plan(20) == [20]
+    assert bench.graph_plan(2000) == [16] * 125
+    assert bench.graph_plan(35) == [18, 17]
+    assert bench.graph_plan(5) == [5]
+    for k in range(1, 400):
+        plan = bench.graph_plan(k)
+        assert sum(plan) == k
+        if k >= 16:
+            assert all(16 <= d <= 31 for d in plan), (k, plan)
