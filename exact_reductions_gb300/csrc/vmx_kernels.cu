@@ -940,7 +940,9 @@ __device__ uint64_t resolve_row(const unsigned char *row, int width, uint64_t S,
 // the row's exact sum and odd count), by their run (from 55 up), else term
 // by term from the samples. The general path; walk_plane_fast() takes the
 // common case in a few passes and falls back here.
-template <typename TS, bool FULL>
+__device__ uint64_t resolve_row_fast(const unsigned char *row, int width, uint64_t S, uint32_t *ctrl);
+
+template <typename TS, bool VEC, bool FULL>
 __device__ uint64_t walk_plane_from(const Params &p, int f, int X, int r, uint64_t S)
 {
     const int H = p.height;
@@ -988,7 +990,9 @@ __device__ uint64_t walk_plane_from(const Params &p, int f, int X, int r, uint64
         }
         r = m;
         if (r < H) {
-            S = resolve_row<TS>(plane + (int64_t)r * p.stride, p.width, S, p.ctrl);
+            const unsigned char *rp = plane + (int64_t)r * p.stride;
+            if (VEC && sizeof(TS) == 2) S = resolve_row_fast(rp, p.width, S, p.ctrl);
+            else S = resolve_row<TS>(rp, p.width, S, p.ctrl);
             count(p.ctrl, kCtrlRowsTerms, 1);
             ++r;
         }
@@ -1297,6 +1301,125 @@ __device__ __forceinline__ void sums64(const uint4 (&V)[8], uint64_t *sum, uint3
     *odd = (ob & 0xffu) + ((ob >> 8) & 0xffu) + ((ob >> 16) & 0xffu) + (ob >> 24);
 }
 
+// Exclusive composition, in lane order, of the lanes' compact runs and of
+// their exact sums; *tot and *tot_s get the warp's.
+__device__ __forceinline__ void warp_excl_lane_run(const LaneRun &x, uint64_t xs, int sh, LaneRun *ex,
+                                                   uint64_t *ex_s, LaneRun *tot, uint64_t *tot_s)
+{
+    const int lane = lane_id();
+    LaneRun v = x;
+    uint64_t vs = xs;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        LaneRun o;
+        o.tlo = __shfl_up_sync(kFull, v.tlo, off);
+        o.d[0] = __shfl_up_sync(kFull, v.d[0], off);
+        o.d[1] = __shfl_up_sync(kFull, v.d[1], off);
+        const uint64_t os = __shfl_up_sync(kFull, vs, off);
+        if (lane >= off) {
+            v = lane_compose(o, v, sh);
+            vs += os;
+        }
+    }
+    tot->tlo = __shfl_sync(kFull, v.tlo, 31);
+    tot->d[0] = __shfl_sync(kFull, v.d[0], 31);
+    tot->d[1] = __shfl_sync(kFull, v.d[1], 31);
+    *tot_s = __shfl_sync(kFull, vs, 31);
+    LaneRun e;
+    e.tlo = __shfl_up_sync(kFull, v.tlo, 1);
+    e.d[0] = __shfl_up_sync(kFull, v.d[0], 1);
+    e.d[1] = __shfl_up_sync(kFull, v.d[1], 1);
+    uint64_t es = __shfl_up_sync(kFull, vs, 1);
+    if (lane == 0) {
+        e = lane_identity();
+        es = 0;
+    }
+    *ex = e;
+    *ex_s = es;
+}
+
+// The terms of a 16-bit row starting on a 16-byte boundary, added to S from
+// term `pos` on, for S from 2^55 up (binade b, last place u = 2^(b-52)), in
+// rounds of 2048 terms: each lane forms the compact run of its 64
+// consecutive terms (eight 8-term runs from eight 16-byte loads, composed in
+// order), the warp composes the lanes' runs in order, and a round whose run
+// keeps S below 2^(b+1) is added at once (ADR-1497 "Decision": a run's
+// increments composed in order; every intermediate sum lies below the final
+// one). Otherwise the first lane whose run takes S there puts its 64 samples
+// in shared memory, the warp composes their one-term runs two per lane, the
+// term that leaves the binade is rounded in full, and the round is taken up
+// again from the next term in the new binade.
+__device__ __noinline__ uint64_t resolve_row_runs(const unsigned char *row, int width, uint64_t S, int pos,
+                                                  uint32_t *ctrl)
+{
+    __shared__ uint32_t swords[kWarps][32];
+    const int lane = lane_id(), wid = (int)(threadIdx.x >> 5);
+    int base = pos & ~2047;
+    while (base < width) {
+        const int b = binade_of(S), sh = b - 52;
+        const uint64_t top = 2ull << b;
+        count(ctrl, kCtrlPasses, 1);
+        const int j0 = base + lane * 64;
+        uint4 V[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) V[v] = load_vec<uint16_t, true>(row, (j0 >> 3) + v, width);
+        if (j0 < pos) mask_before(V, j0, pos);  // terms before pos are already in S
+        LaneRun lr = lane_identity();
+        uint64_t ls = 0;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            uint32_t t[8];
+            const uint32_t w4[4] = {V[v].x, V[v].y, V[v].z, V[v].w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) terms_of_word(w4[w], &t[2 * w], &t[2 * w + 1]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ls += t[i];
+            lr = lane_compose(lr, lane_run_fp2(t, sh), sh);
+        }
+        LaneRun ex, tot;
+        uint64_t ex_s, tot_s;
+        warp_excl_lane_run(lr, ls, sh, &ex, &ex_s, &tot, &tot_s);
+        const uint64_t whole = apply(lane_to_run(tot, tot_s), S, sh);
+        if (whole < top) {
+            S = whole;
+            base += 32 * 64;
+            pos = base;
+            continue;
+        }
+        const uint64_t sb = apply(lane_to_run(ex, ex_s), S, sh);
+        const uint64_t sa = apply(lane_to_run(lr, ls), sb, sh);
+        const int src = __ffs(__ballot_sync(kFull, sa >= top)) - 1;
+        const uint64_t s_src = __shfl_sync(kFull, sb, src);
+        if (lane == src) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                swords[wid][4 * v] = V[v].x;
+                swords[wid][4 * v + 1] = V[v].y;
+                swords[wid][4 * v + 2] = V[v].z;
+                swords[wid][4 * v + 3] = V[v].w;
+            }
+        }
+        __syncwarp();
+        const uint32_t w = swords[wid][lane];
+        __syncwarp();
+        const uint64_t t0 = term_of_sample(w & 0xffffu), t1 = term_of_sample(w >> 16);
+        const Run r0 = run_of_term(t0, sh), r1 = run_of_term(t1, sh);
+        Run tot2;
+        const Run ex2 = warp_excl_run(compose(r0, r1, sh), sh, &tot2);
+        const uint64_t c0 = apply(ex2, s_src, sh);
+        const uint64_t c1 = apply(r0, c0, sh);
+        const bool bad0 = c1 >= top;
+        const bool bad1 = !bad0 && apply(r1, c1, sh) >= top;
+        const int src2 = __ffs(__ballot_sync(kFull, bad0 || bad1)) - 1;
+        const bool second = __shfl_sync(kFull, (int)bad1, src2);
+        const uint64_t before = __shfl_sync(kFull, bad0 ? c0 : c1, src2);
+        const uint64_t tm = __shfl_sync(kFull, bad0 ? t0 : t1, src2);
+        S = rnd53(before + tm);  // the term that leaves the binade, rounded in full
+        pos = base + src * 64 + 2 * src2 + (second ? 1 : 0) + 1;
+    }
+    return S;
+}
+
 // The terms of a 16-bit row starting on a 16-byte boundary, added to S from
 // term `pos` on, in rounds of 2048 terms (64 consecutive terms per lane, from
 // eight 16-byte loads). A round that keeps S at or below 2^53, or in its
@@ -1312,7 +1435,7 @@ __device__ uint64_t resolve_row_fast(const unsigned char *row, int width, uint64
     const int lane = lane_id(), wid = (int)(threadIdx.x >> 5);
     int base = 0, pos = 0;
     while (base < width) {
-        if (S >= kTwo53 && binade_of(S) >= 55) return resolve_row<uint16_t>(row, width, S, ctrl, pos);
+        if (S >= kTwo53 && binade_of(S) >= 55) return resolve_row_runs(row, width, S, pos, ctrl);
         count(ctrl, kCtrlPasses, 1);
         const int j0 = base + lane * 64;
         uint4 V[8];
@@ -1433,7 +1556,7 @@ __device__ uint64_t walk_plane_fast(const Params &p, int f, int X, Agg *t)
             return Sn;
         }
     }
-    return walk_plane_from<TS, FULL>(p, f, X, row + 1, S);
+    return walk_plane_from<TS, VEC, FULL>(p, f, X, row + 1, S);
 }
 
 // One part of a frame's results: part 0 and 1 the moments of ref and dis
