@@ -379,17 +379,18 @@ def run_ours(args, rank, local_rank, world, pg):
     stream = torch.cuda.current_stream(dev)
     kernels_per_step = 1
 
-    for _ in range(max(args.warmup, 3)):
-        for fg, _ in graphs:
-            fg.replay()
-    torch.cuda.synchronize()
-    assert all(fg.status() == 0 for fg, _ in graphs), "bounded device wait gave up"
-
     schedule = [fg for fg, n in graphs for _ in range(n)]
     starts = [torch.cuda.Event(enable_timing=True) for _ in schedule]
     ends = [torch.cuda.Event(enable_timing=True) for _ in schedule]
 
     with Clocks(local_rank) as clocks:
+        # The warm-up runs once the clock sampler is up, so that the timed
+        # steps start on a busy GPU rather than after its pause.
+        for _ in range(max(args.warmup, 3)):
+            for fg, _ in graphs:
+                fg.replay()
+        torch.cuda.synchronize()
+        assert all(fg.status() == 0 for fg, _ in graphs), "bounded device wait gave up"
         if pg is not None:
             dist.barrier(group=pg)
         torch.cuda.synchronize()

@@ -19,6 +19,7 @@ VMX_ENOMEM = -2
 VMX_ECUDA = -3
 VMX_ETIMEOUT = -4
 VMX_ESCRATCH = -5
+VMX_ECHECK = -6
 NOALLOC_SCRATCH_BYTES = 16 << 20
 FEATURE_MOMENT = 1
 FEATURE_PSNR = 2
@@ -51,6 +52,8 @@ SIGNATURES = {
     "vmx_frames_host_traffic": (None, [_i32, _i32, _i64, _i32, _i32, _i32, _i32, _vp, _vp]),
     "vmx_frames_noalloc": (_i32, [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _vp, _vp, _vp,
                                   _vp, _vp, _vp, _vp, _vp]),
+    "vmx_checked_build": (_i32, []),
+    "vmx_check_status": (_i32, [_vp]),
     "vmx_strerror": (ctypes.c_char_p, [_i32]),
     "vmx_kernel_launches": (_u64, []),
     "vmx_version": (_i32, []),

@@ -57,6 +57,23 @@ bool wait_stall_setting()
     return v && std::strcmp(v, "1") == 0;
 }
 
+// Tests of a checked build: VMX_TEST_CHECK_SHRINK=1 makes the kernel take the
+// per-plane row arrays as one element shorter than they are, so that an
+// index check fails (and skips its access; nothing goes out of bounds).
+uint32_t check_shrink_setting()
+{
+    const char *v = std::getenv("VMX_TEST_CHECK_SHRINK");
+    return v && std::strcmp(v, "1") == 0 ? 1u : 0u;
+}
+
+// A device status word: bit 1 an index check failed (checked builds), bit 0
+// a bounded wait gave up.
+int status_of_word(uint32_t w)
+{
+    if (w & 2u) return VMX_ECHECK;
+    return w != 0u ? VMX_ETIMEOUT : VMX_OK;
+}
+
 // Tests of forward progress: VMX_TEST_GRID_MULT=n (2..16) launches n times
 // as many CTAs as the GPU holds at once, so that most of the grid starts only
 // as earlier CTAs exit.
@@ -197,6 +214,7 @@ int run_frames(const void *ref, const void *dis, int width, int height, int64_t 
     p.spin_limit = spin_limit_setting();
     p.test_stall = wait_stall_setting() ? 1u : 0u;
     p.test_grid_mult = grid_mult_setting();
+    p.check_shrink = check_shrink_setting();
     p.overlap = (flags & VMX_FLAG_OVERLAP) ? 1u : 0u;
     const bool vec = (uintptr_t)ref % 16 == 0 && (uintptr_t)dis % 16 == 0 && stride % 16 == 0;
     err = (flags & VMX_FLAG_CLEARED) ? cudaSuccess
@@ -215,7 +233,7 @@ int run_frames(const void *ref, const void *dis, int width, int height, int64_t 
     if (err == cudaSuccess) err = ferr;
     if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
     if (err != cudaSuccess) status = cuda_fail(err);
-    else if (dev_status) status = VMX_ETIMEOUT;
+    else status = status_of_word(dev_status);
     return status;
 }
 
@@ -226,7 +244,18 @@ using namespace vmx;
 
 extern "C" {
 
-int vmx_version(void) { return 10000; }
+int vmx_version(void) { return 10100; }
+
+int vmx_checked_build(void) { return VMX_CHECK ? 1 : 0; }
+
+int vmx_check_status(void *stream)
+{
+    if (!VMX_CHECK) return VMX_OK;
+    uint32_t v = 0;
+    const cudaError_t err = integer_psnr_check_flags(&v, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err);
+    return v ? VMX_ECHECK : VMX_OK;
+}
 
 uint64_t vmx_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -239,6 +268,7 @@ const char *vmx_strerror(int status)
     case VMX_ECUDA: return g_last_cuda[0] ? g_last_cuda : "CUDA error";
     case VMX_ETIMEOUT: return "a bounded device wait gave up";
     case VMX_ESCRATCH: return "shape needs more scratch than the no-alloc call holds";
+    case VMX_ECHECK: return "an index check failed (checked build)";
     default: return "unknown status";
     }
 }
@@ -295,6 +325,7 @@ int vmx_integer_psnr_frames(const void *ref, const void *dis, int width, int hei
     a.sse = sse;
     a.mse = mse;
     a.rows = rows;
+    a.check_shrink = check_shrink_setting();
     const cudaError_t err = launch_integer_psnr(a, static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) return cuda_fail(err);
     g_launches.fetch_add(2, std::memory_order_relaxed);
@@ -345,7 +376,7 @@ int vmx_workspace_status(const void *workspace, void *stream)
     cudaError_t err = cudaMemcpyAsync(&v, ctrl + kCtrlStatus, sizeof v, cudaMemcpyDeviceToHost, s);
     if (err == cudaSuccess) err = cudaStreamSynchronize(s);
     if (err != cudaSuccess) return cuda_fail(err);
-    return v ? VMX_ETIMEOUT : VMX_OK;
+    return status_of_word(v);
 }
 
 int vmx_workspace_stats(const void *workspace, void *stream, uint64_t *out4)
@@ -585,7 +616,7 @@ int vmx_frames_host(const void *ref, const void *dis, int width, int height,
     if (err == cudaSuccess && status == VMX_OK)
         err = cudaMemcpyAsync(&st, dstatus, sizeof st, cudaMemcpyDeviceToHost, cs);
     if (err == cudaSuccess) err = cudaStreamSynchronize(cs);
-    if (err == cudaSuccess && status == VMX_OK && st) status = VMX_ETIMEOUT;
+    if (err == cudaSuccess && status == VMX_OK && st) status = status_of_word(st);
     if (copy) cudaStreamSynchronize(copy);
     for (int s = 0; s < 2; ++s) {
         if (copied[s]) cudaEventDestroy(copied[s]);

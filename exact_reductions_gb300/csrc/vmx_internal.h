@@ -66,6 +66,13 @@ constexpr uint32_t kPipeSpinLimit = 1u << 20;  // polls of one chunk's barrier, 
 #define VMX_FIRST_UNROLL 16
 #endif
 constexpr int kFirstUnroll = VMX_FIRST_UNROLL;  // loads in flight per lane in the walks' sequential sums
+#ifndef VMX_CHECK
+// 1: a checked build (a test variant). Every index the kernels compute into
+// one of their arrays is compared with the array's extent first; one out of
+// range sets bit 1 of the call's status word (VMX_ECHECK on the host) and the
+// access is skipped. Nothing traps. 0: the checks compile to nothing.
+#define VMX_CHECK 0
+#endif
 #ifndef VMX_WHOLE_LOADS
 #define VMX_WHOLE_LOADS 1  // passes wholly inside a row load without per-vector checks
 #endif
@@ -142,6 +149,7 @@ struct Params {
     uint32_t overlap; // launched to overlap the previous kernel on the stream
     uint32_t test_stall;  // tests only: the walks wait for a count never reached
     int test_grid_mult;   // tests only (host side): launch this many times the resident CTAs
+    uint32_t check_shrink;  // tests of a checked build: the row-sum arrays' extent is taken as one less
 };
 
 // Enqueue the frame kernel. `features` VMX_FEATURE_* bits; `vec` true when

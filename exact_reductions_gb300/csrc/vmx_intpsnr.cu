@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include "vmx.h"
+#include "vmx_internal.h"
 #include "vmx_intpsnr.h"
 
 namespace vmx {
@@ -26,6 +27,25 @@ namespace {
 
 constexpr unsigned kAll = 0xffffffffu;
 constexpr int kPsnrThreads = 256;
+
+// Failed index checks of a checked build (bit 1), per device; read and
+// cleared by integer_psnr_check_flags().
+__device__ uint32_t g_check_flags;
+
+// With VMX_CHECK: whether i < n; if not, the failure is recorded and the
+// caller skips the access. Without: always true.
+__device__ __forceinline__ bool in_extent(size_t i, size_t n)
+{
+#if VMX_CHECK
+    if (i < n) return true;
+    atomicOr(&g_check_flags, 2u);
+    return false;
+#else
+    (void)i;
+    (void)n;
+    return true;
+#endif
+}
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *ptr)
 {
@@ -118,7 +138,7 @@ __global__ void __launch_bounds__(kPsnrThreads) sse_kernel(const unsigned char *
                                                            const unsigned char *dis, int width,
                                                            int height, int64_t stride, int frames,
                                                            unsigned long long *sse,
-                                                           uint64_t *rows)
+                                                           uint64_t *rows, uint32_t shrink)
 {
     const int lane = (int)(threadIdx.x & 31);
     const int64_t nrows = (int64_t)frames * height;
@@ -126,11 +146,13 @@ __global__ void __launch_bounds__(kPsnrThreads) sse_kernel(const unsigned char *
     for (int64_t w = (int64_t)blockIdx.x * (kPsnrThreads / 32) + (threadIdx.x >> 5); w < nrows;
          w += warps) {
         const int f = (int)(w / height);
+        if (!in_extent((size_t)w, (size_t)nrows)) continue;  // the row lies inside the planes
         const int64_t off = w * stride;  // row w of the batch: frame f, row w - f * height
         const uint64_t row = warp_total(lane_sse<BYTES, VEC>(ref + off, dis + off, width, lane));
         if (lane == 0) {
-            if (rows) rows[w] = row;
-            atomicAdd(sse + f, (unsigned long long)row);
+            // (a test of a checked build takes the rows' extent as one less)
+            if (rows && in_extent((size_t)w, (size_t)nrows - shrink)) rows[w] = row;
+            if (in_extent((size_t)f, (size_t)frames)) atomicAdd(sse + f, (unsigned long long)row);
         }
     }
 }
@@ -147,15 +169,27 @@ cudaError_t launch_sse(const IntPsnrArgs &a, bool vec, int grid, cudaStream_t s)
     if (vec)
         sse_kernel<BYTES, true><<<grid, kPsnrThreads, 0, s>>>(
             a.ref, a.dis, a.width, a.height, a.stride, a.frames,
-            reinterpret_cast<unsigned long long *>(a.sse), a.rows);
+            reinterpret_cast<unsigned long long *>(a.sse), a.rows, a.check_shrink);
     else
         sse_kernel<BYTES, false><<<grid, kPsnrThreads, 0, s>>>(
             a.ref, a.dis, a.width, a.height, a.stride, a.frames,
-            reinterpret_cast<unsigned long long *>(a.sse), a.rows);
+            reinterpret_cast<unsigned long long *>(a.sse), a.rows, a.check_shrink);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t integer_psnr_check_flags(uint32_t *flags, cudaStream_t stream)
+{
+    *flags = 0;
+    if (!VMX_CHECK) return cudaSuccess;
+    cudaError_t err = cudaMemcpyFromSymbolAsync(flags, g_check_flags, sizeof(uint32_t), 0,
+                                                cudaMemcpyDeviceToHost, stream);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+    const uint32_t zero = 0;
+    if (err == cudaSuccess) err = cudaMemcpyToSymbol(g_check_flags, &zero, sizeof zero);
+    return err;
+}
 
 cudaError_t launch_integer_psnr(const IntPsnrArgs &a, cudaStream_t stream)
 {

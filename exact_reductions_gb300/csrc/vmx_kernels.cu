@@ -92,6 +92,31 @@ __device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gp
 
 
 
+// --------------------------------------------------------- checked builds ---
+// With VMX_CHECK, chk() compares an index with its array's extent and, when it
+// is out of range, sets bit 1 of the call's status word and returns false so
+// that the access is skipped (a load gives 0). Without, it is always true.
+#if VMX_CHECK
+__device__ __forceinline__ bool chk(uint32_t *status, size_t i, size_t n)
+{
+    if (i < n) return true;
+    atomicOr(status, 2u);
+    return false;
+}
+#else
+__device__ __forceinline__ bool chk(uint32_t *, size_t, size_t) { return true; }
+#endif
+
+// Extents (elements) of the kernel's arrays; a test of a checked build takes
+// the per-plane row arrays' as one less, so that a check fires.
+__device__ __forceinline__ size_t ext_plane_rows(const Params &p)
+{
+    return (size_t)p.frames * 2 * p.height - p.check_shrink;
+}
+__device__ __forceinline__ size_t ext_frame_rows(const Params &p) { return (size_t)p.frames * p.height; }
+__device__ __forceinline__ size_t ext_items(const Params &p) { return (size_t)p.frames * p.items_per_frame; }
+__device__ __forceinline__ size_t ext_blocks(const Params &p) { return (size_t)p.frames * p.blocks_per_frame; }
+
 // Sample type traits: a 16-byte vector holds 8 uint16 or 16 uint8 samples.
 template <typename TS>
 struct Samples;
@@ -552,6 +577,10 @@ __device__ RowSums row_sums16(const unsigned char *rr, const unsigned char *dr, 
             const uint4 *vd = reinterpret_cast<const uint4 *>(dr) + base + lane;
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
+                if (VMX_CHECK && !chk(status, base + 32 * u + lane, nfull)) {
+                    R[u] = D[u] = make_uint4(0u, 0u, 0u, 0u);
+                    continue;
+                }
                 R[u] = ld_nc_v4(vr + 32 * u);
                 D[u] = ld_nc_v4(vd + 32 * u);
             }
@@ -946,16 +975,20 @@ template <typename TS, bool VEC, bool FULL>
 __device__ uint64_t walk_plane_from(const Params &p, int f, int X, int r, uint64_t S)
 {
     const int H = p.height;
-    const size_t off = ((size_t)f * 2 + X) * H;
+    const size_t off = ((size_t)f * 2 + X) * H, nrows = ext_plane_rows(p);
     const uint64_t *R = p.s2_rows + off;
     const uint32_t *O = p.odd_rows + off;
     const RowRec *rec = p.rec + off;
     const unsigned char *plane = (X == 0 ? p.ref : p.dis) + (int64_t)f * p.pitch;
+    const auto ldR = [&p, R, off, nrows](int i) { return chk(p.status, off + i, nrows) ? __ldcg(R + i) : 0ull; };
+    const auto ldO = [&p, O, off, nrows](int i) {
+        return chk(p.status, off + i, nrows) ? (uint64_t)__ldcg(O + i) : 0ull;
+    };
     while (r < H) {
         int m;
         if (S < kTwo53) {
             SC before;
-            m = warp_first([R](int i) { return SC{__ldcg(R + i), 0}; }, r, H,
+            m = warp_first([&ldR](int i) { return SC{ldR(i), 0}; }, r, H,
                            [S](SC x) { return S + x.s > kTwo53; }, &before, p.ctrl);
             S += before.s;
             count(p.ctrl, kCtrlRowsExact, (uint32_t)(m - r));
@@ -963,7 +996,7 @@ __device__ uint64_t walk_plane_from(const Params &p, int f, int X, int r, uint64
             const int b = binade_of(S);
             const uint64_t top = 2ull << b;
             SC before;
-            m = warp_first([R, O](int i) { return SC{__ldcg(R + i), (uint64_t)__ldcg(O + i)}; }, r, H,
+            m = warp_first([&ldR, &ldO](int i) { return SC{ldR(i), ldO(i)}; }, r, H,
                            [S, b, top](SC x) { return closed_form_after(S, x.s, x.c, b) >= top; },
                            &before, p.ctrl);
             S = closed_form_after(S, before.s, before.c, b);
@@ -971,13 +1004,15 @@ __device__ uint64_t walk_plane_from(const Params &p, int f, int X, int r, uint64
         } else if (FULL) {
             const int b = binade_of(S);
             m = warp_run_walk(
-                [R, rec, b](int i, int sh, bool *ok) {
-                    const uint64_t rs = __ldcg(R + i);
+                [&p, &ldR, rec, off, nrows, b](int i, int sh, bool *ok) {
+                    const uint64_t rs = ldR(i);
                     if (rs == 0) {
                         *ok = true;
                         return run_identity();
                     }
-                    const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(rec + i));
+                    const uint4 w = chk(p.status, off + i, nrows)
+                                        ? __ldcg(reinterpret_cast<const uint4 *>(rec + i))
+                                        : make_uint4(0u, 0u, 0u, 0u);
                     const uint64_t inc0 = ((uint64_t)w.y << 32) | w.x;
                     const int e = (int)(w.w & 0xffu), kind = (int)((w.w >> 8) & 0xffu);
                     *ok = kind == kRowRun && e == b;
@@ -1000,27 +1035,33 @@ __device__ uint64_t walk_plane_from(const Params &p, int f, int X, int r, uint64
     return S;
 }
 
-// The CPU's psnr noise in units: the exact row sums added in row order.
-__device__ uint64_t walk_rows(const uint64_t *rows, int H, uint32_t *ctrl)
+// The CPU's psnr noise of frame f in units: the exact row sums added in
+// row order.
+__device__ uint64_t walk_rows(const Params &p, int f)
 {
+    const int H = p.height;
+    const size_t off = (size_t)f * H, n = ext_frame_rows(p);
+    const uint64_t *rows = p.psnr_rows + off;
+    uint32_t *ctrl = p.ctrl;
+    const auto ld = [&p, rows, off, n](int i) { return chk(p.status, off + i, n) ? __ldcg(rows + i) : 0ull; };
     uint64_t S = 0;
     int r = 0;
     while (r < H) {
         int m;
         if (S < kTwo53) {
             SC before;
-            m = warp_first([rows](int i) { return SC{__ldcg(rows + i), 0}; }, r, H,
+            m = warp_first([&ld](int i) { return SC{ld(i), 0}; }, r, H,
                            [S](SC x) { return S + x.s > kTwo53; }, &before, ctrl);
             S += before.s;
         } else {
             m = warp_run_walk(
-                [rows](int i, int sh, bool *ok) {
+                [&ld](int i, int sh, bool *ok) {
                     *ok = true;
-                    return run_of_term(__ldcg(rows + i), sh);
+                    return run_of_term(ld(i), sh);
                 },
                 r, H, S, ctrl);
         }
-        if (m < H) S = rnd53(S + __ldcg(rows + m));
+        if (m < H) S = rnd53(S + ld(m));
         r = m + 1;
     }
     return S;
@@ -1057,14 +1098,16 @@ __device__ __forceinline__ uint32_t block_items(const Params &p, int b)
 // wrote the record, then set the block's count one past its items (release).
 __device__ __forceinline__ bool block_done(const Params &p, int f, int b)
 {
-    return ld_acquire(p.block_fin + (size_t)f * p.blocks_per_frame + b) == block_items(p, b) + 1u;
+    const size_t i = (size_t)f * p.blocks_per_frame + b;
+    return chk(p.status, i, ext_blocks(p)) && ld_acquire(p.block_fin + i) == block_items(p, b) + 1u;
 }
 
 // Whether item i of frame f has its record out (its flag is 1, or 2 once the
 // look-back has published its inclusive prefix).
 __device__ __forceinline__ bool item_done(const Params &p, int f, int i)
 {
-    return ld_acquire(p.flags + (size_t)f * p.items_per_frame + i) != 0u;
+    const size_t k = (size_t)f * p.items_per_frame + i;
+    return chk(p.status, k, ext_items(p)) && ld_acquire(p.flags + k) != 0u;
 }
 
 // Called by the whole warp of block b's last item to finish, after lane 0
@@ -1078,7 +1121,7 @@ __device__ __noinline__ void fold_block(const Params &p, int f, int b)
     const int lane = lane_id(), I = p.items_per_frame;
     const int i = b * kBlockItems + lane;
     Agg g = agg_zero();
-    if (lane < (int)block_items(p, b)) {
+    if (lane < (int)block_items(p, b) && chk(p.status, (size_t)f * I + i, ext_items(p))) {
         const Agg *it = p.items + (size_t)f * I + i;
         g.s2[0] = __ldcg(&it->s2[0]);
         g.s2[1] = __ldcg(&it->s2[1]);
@@ -1094,9 +1137,10 @@ __device__ __noinline__ void fold_block(const Params &p, int f, int b)
     t.s1[1] = warp_sum_lt51(g.s1[1]);
     t.psnr = warp_sum_lt51(g.psnr);
     t.odd = warp_sum_lt51(g.odd);  // two counts below 2^17, summed in their halves
-    if (lane == 0) {
-        store_agg(p.blocks + (size_t)f * p.blocks_per_frame + b, t);
-        st_release(p.block_fin + (size_t)f * p.blocks_per_frame + b, block_items(p, b) + 1u);
+    const size_t k = (size_t)f * p.blocks_per_frame + b;
+    if (lane == 0 && chk(p.status, k, ext_blocks(p))) {
+        store_agg(p.blocks + k, t);
+        st_release(p.block_fin + k, block_items(p, b) + 1u);
     }
 }
 
@@ -1123,6 +1167,7 @@ __device__ Agg frame_totals(const Params &p, int f, int part)
         const int X = part;
         uint64_t s2 = 0, s1 = 0, odd = 0;
         for (int b = lane; b < NB; b += 32) {
+            if (!chk(p.status, (size_t)f * NB + b, ext_blocks(p))) continue;
             s2 += __ldcg(&bl[b].s2[X]);
             s1 += __ldcg(&bl[b].s1[X]);
             odd += __ldcg(&bl[b].odd);
@@ -1132,7 +1177,8 @@ __device__ Agg frame_totals(const Params &p, int f, int part)
         t.odd = warp_sum(odd);
     } else {
         uint64_t ps = 0;
-        for (int b = lane; b < NB; b += 32) ps += __ldcg(&bl[b].psnr);
+        for (int b = lane; b < NB; b += 32)
+            if (chk(p.status, (size_t)f * NB + b, ext_blocks(p))) ps += __ldcg(&bl[b].psnr);
         t.psnr = warp_sum(ps);
     }
     return t;
@@ -1178,6 +1224,7 @@ __device__ int crossing_item(const Params &p, int f, int X, SC *before)
     const auto sums = [X, shift](const Agg *a) {
         return SC{__ldcg(&a->s2[X]), (__ldcg(&a->odd) >> shift) & 0xffffffffull};
     };
+    const size_t nb = ext_blocks(p), ni = ext_items(p);
     SC run{0, 0};  // exact prefix of blocks [0, base), all complete
     int base = 0;
     uint32_t spins = 0;
@@ -1188,12 +1235,13 @@ __device__ int crossing_item(const Params &p, int f, int X, SC *before)
         SC v{0, 0};
         if (b < NB) {
             done = block_done(p, f, b);
-            if (done) v = sums(bl + b);
+            if (done && chk(p.status, (size_t)f * NB + b, nb)) v = sums(bl + b);
         }
         const WindowScan w = scan_window(done, v, run);
         if (w.hit >= 0) {  // a complete block: every item in it is out
             const int i = (base + w.hit) * kBlockItems + lane;
-            const WindowScan wi = scan_window(true, i < I ? sums(it + i) : SC{0, 0}, w.before);
+            const WindowScan wi = scan_window(
+                true, i < I && chk(p.status, (size_t)f * I + i, ni) ? sums(it + i) : SC{0, 0}, w.before);
             *before = wi.before;
             return (base + w.hit) * kBlockItems + wi.hit;
         }
@@ -1217,7 +1265,7 @@ __device__ int crossing_item(const Params &p, int f, int X, SC *before)
             SC vi{0, 0};
             if (i < I) {
                 di = item_done(p, f, i);
-                if (di) vi = sums(it + i);
+                if (di && chk(p.status, (size_t)f * I + i, ni)) vi = sums(it + i);
             }
             const WindowScan wi = scan_window(di, vi, run);
             if (wi.hit >= 0) {
@@ -1518,9 +1566,12 @@ template <typename TS, bool VEC, bool FULL>
 __device__ uint64_t walk_plane_fast(const Params &p, int f, int X, Agg *t)
 {
     const int I = p.items_per_frame, H = p.height;
-    const size_t off = ((size_t)f * 2 + X) * H;
+    const size_t off = ((size_t)f * 2 + X) * H, nrows = ext_plane_rows(p);
     const uint64_t *R = p.s2_rows + off;
     const uint32_t *O = p.odd_rows + off;
+    const auto ldRO = [&p, R, O, off, nrows](int i) {
+        return chk(p.status, off + i, nrows) ? SC{__ldcg(R + i), (uint64_t)__ldcg(O + i)} : SC{0, 0};
+    };
     SC pre_items;
     const int it = crossing_item<FULL>(p, f, X, &pre_items);
     if (it >= I) {
@@ -1532,8 +1583,7 @@ __device__ uint64_t walk_plane_fast(const Params &p, int f, int X, Agg *t)
     const int r0 = it * p.rows_per_item;
     const int row = p.rows_per_item == 1  // the item is the row
                         ? r0
-                        : warp_first([R, O](int i) { return SC{__ldcg(R + i), (uint64_t)__ldcg(O + i)}; },
-                                     r0, min(H, r0 + p.rows_per_item),
+                        : warp_first(ldRO, r0, min(H, r0 + p.rows_per_item),
                                      [pre_items](SC x) { return pre_items.s + x.s > kTwo53; }, &b2,
                                      p.ctrl);
     const SC pre = sc_add(pre_items, b2);
@@ -1544,7 +1594,8 @@ __device__ uint64_t walk_plane_fast(const Params &p, int f, int X, Agg *t)
     if (VEC && sizeof(TS) == 2) S = resolve_row_fast(rp, p.width, S, p.ctrl);
     else S = resolve_row<TS>(rp, p.width, S, p.ctrl);
     count(p.ctrl, kCtrlRowsTerms, 1);
-    const uint64_t rs = __ldcg(R + row), rc = __ldcg(O + row);
+    const SC rsc = ldRO(row);
+    const uint64_t rs = rsc.s, rc = rsc.c;
     *t = frame_totals(p, f, X);
     const uint64_t tot = t->s2[X], tot_odd = X ? (t->odd >> 32) : (t->odd & 0xffffffffull);
     const uint64_t rest_s = tot - pre.s - rs, rest_c = tot_odd - pre.c - rc;
@@ -1577,7 +1628,7 @@ __device__ __noinline__ void walk_part(const Params &p, int f, int part)
             s2 = t.s2[X];
             count(p.ctrl, kCtrlRowsExact, (uint32_t)p.height);
         }
-        if (lead) {
+        if (lead && chk(p.status, (size_t)f * 4 + 2 + X, (size_t)p.frames * 4)) {
             p.moments[(size_t)f * 4 + X] = scaled_mean(t.s1[X], p.k, N);
             p.moments[(size_t)f * 4 + 2 + X] = scaled_mean(s2, 2 * p.k, N);
             if (p.s2_sums) p.s2_sums[(size_t)f * 2 + X] = s2;
@@ -1585,8 +1636,8 @@ __device__ __noinline__ void walk_part(const Params &p, int f, int part)
     } else if (P) {
         const Agg t = frame_totals(p, f, 2);
         const uint64_t d = t.psnr <= kTwo53 ? t.psnr
-                                            : walk_rows(p.psnr_rows + (size_t)f * p.height, p.height, p.ctrl);
-        if (lead) {
+                                            : walk_rows(p, f);
+        if (lead && chk(p.status, (size_t)f, (size_t)p.frames)) {
             p.mse[f] = scaled_mean(d, 2 * p.k, N);
             if (p.noise_sums) p.noise_sums[f] = d;
         }
@@ -1614,7 +1665,8 @@ __device__ __noinline__ void lookback(const Params &p, int f, int j, uint64_t ag
         uint32_t spins = 0;
         for (;;) {
             const int i = q - lane;  // lane 0 the nearest predecessor
-            const uint32_t fl = i >= 0 ? ld_acquire(p.flags + base + i) : 2u;
+            const uint32_t fl =
+                i < 0 ? 2u : (chk(p.status, base + i, ext_items(p)) ? ld_acquire(p.flags + base + i) : 2u);
             const unsigned zero = __ballot_sync(kFull, fl == 0u);
             const unsigned incl = __ballot_sync(kFull, fl == 2u);
             const int fz = zero ? __ffs(zero) - 1 : 32;
@@ -1628,7 +1680,8 @@ __device__ __noinline__ void lookback(const Params &p, int f, int j, uint64_t ag
                 continue;
             }
             uint64_t vr = 0, vd = 0;
-            if (i >= 0 && lane < fi) {
+            if (i >= 0 && !chk(p.status, base + i, ext_items(p))) {
+            } else if (i >= 0 && lane < fi) {
                 vr = __ldcg(&p.items[base + i].s2[0]);
                 vd = __ldcg(&p.items[base + i].s2[1]);
             } else if (i >= 0 && lane == fi) {
@@ -1641,7 +1694,7 @@ __device__ __noinline__ void lookback(const Params &p, int f, int j, uint64_t ag
             q -= 32;
         }
     }
-    if (lane == 0) {
+    if (lane == 0 && chk(p.status, idx, ext_items(p))) {
         __stcg(p.item_inc + idx * 2, pr + aggr);
         __stcg(p.item_inc + idx * 2 + 1, pd + aggd);
         st_release(p.flags + idx, 2u);
@@ -1741,30 +1794,30 @@ __global__ void __maxnreg__(kMaxRegs) frames_kernel(Params p)
         // the warp's shared slots, so that no item totals stay live in
         // registers across rows; lane i reads row i's back afterwards.
         for (int r = r0; r < r1; ++r) {
+            // (a checked build: the row and the frame lie inside the planes)
+            if (!chk(p.status, (size_t)f * H + r, ext_frame_rows(p))) continue;
             const unsigned char *rr = fr + (int64_t)r * p.stride;
             const unsigned char *dr = fd + (int64_t)r * p.stride;
             const RowSums rs = sizeof(TS) == 2
                                    ? row_sums16<M, P, ODD, VEC, STG, LOW>(rr, dr, p.width, pp, src, p.status)
                                    : row_sums8<M, P, VEC>(rr, dr, p.width);
             if (lane == 0) {
-                if (M) {
-                    p.s2_rows[((size_t)f * 2) * H + r] = rs.t2r;
-                    p.s2_rows[((size_t)f * 2 + 1) * H + r] = rs.t2d;
-                }
-                if (ODD) {
-                    p.odd_rows[((size_t)f * 2) * H + r] = rs.oddr;
-                    p.odd_rows[((size_t)f * 2 + 1) * H + r] = rs.oddd;
-                }
-                if (P) p.psnr_rows[(size_t)f * H + r] = rs.tp;
+                const size_t k0 = ((size_t)f * 2) * H + r, k1 = ((size_t)f * 2 + 1) * H + r;
+                const size_t np = ext_plane_rows(p);
+                if (M && chk(p.status, k0, np)) p.s2_rows[k0] = rs.t2r;
+                if (M && chk(p.status, k1, np)) p.s2_rows[k1] = rs.t2d;
+                if (ODD && chk(p.status, k0, np)) p.odd_rows[k0] = rs.oddr;
+                if (ODD && chk(p.status, k1, np)) p.odd_rows[k1] = rs.oddd;
+                if (P) p.psnr_rows[(size_t)f * H + r] = rs.tp;  // (f, r) checked above
             }
-            if (lane == 0)
+            if (lane == 0 && chk(p.status, r - r0, kMaxRowsPerItem))
                 item_rows[wid][r - r0] = RowSlot{rs.t2r, rs.t2d, rs.tp, (uint64_t)rs.oddr | ((uint64_t)rs.oddd << 32),
                                                  rs.s1r | (rs.s1d << 32)};
         }
         __syncwarp();
         uint64_t my_r = 0, my_d = 0, my_p = 0, my_o = 0;  // this lane's row of the item
         uint32_t s1r = 0, s1d = 0;
-        if (lane < r1 - r0) {
+        if (lane < r1 - r0 && chk(p.status, lane, kMaxRowsPerItem)) {
             const RowSlot v = item_rows[wid][lane];
             my_r = v.x;
             my_d = v.y;
@@ -1790,7 +1843,7 @@ __global__ void __maxnreg__(kMaxRegs) frames_kernel(Params p)
             g.odd = my_o;
         }
         if (P) g.psnr = one ? my_p : warp_sum_lt51(my_p);
-        if (lane == 0) {
+        if (lane == 0 && chk(p.status, (size_t)f * I + j, ext_items(p))) {
             Agg *ia = p.items + (size_t)f * I + j;
             store_agg(ia, g);
             // The look-back reads each item's flag: its sums are out.
@@ -1820,7 +1873,8 @@ __global__ void __maxnreg__(kMaxRegs) frames_kernel(Params p)
                         rec.e = (uint8_t)e;
                         rec.kind = kRowRun;
                     }
-                    if (lane == 0) p.rec[((size_t)f * 2 + X) * H + r] = rec;
+                    const size_t k = ((size_t)f * 2 + X) * H + r;
+                    if (lane == 0 && chk(p.status, k, ext_plane_rows(p))) p.rec[k] = rec;
                 }
             }
         }
@@ -1836,7 +1890,9 @@ __global__ void __maxnreg__(kMaxRegs) frames_kernel(Params p)
             uint32_t last = 0;
             if (lane == 0) {
                 uint32_t *cnt = p.block_fin + (size_t)f * NB + b;
-                const uint32_t old = FULL ? atom_add_acq_rel(cnt, 1u) : atom_add_release(cnt, 1u);
+                const uint32_t old = !chk(p.status, (size_t)f * NB + b, ext_blocks(p)) ? 0u
+                                     : FULL ? atom_add_acq_rel(cnt, 1u)
+                                            : atom_add_release(cnt, 1u);
                 last = old + 1u == block_items(p, b) + p.test_stall ? 1u : 0u;
                 if (last && !FULL) fence_acq_rel();
             }

@@ -55,6 +55,7 @@ extern "C" {
 #define VMX_ECUDA (-3)     /* a CUDA call failed; vmx_strerror() names it */
 #define VMX_ETIMEOUT (-4)  /* a bounded device wait gave up; outputs are not valid */
 #define VMX_ESCRATCH (-5)  /* the shape needs more than VMX_NOALLOC_SCRATCH_BYTES */
+#define VMX_ECHECK (-6)    /* a checked build only: an index check failed (the access was skipped) */
 
 #define VMX_FEATURE_MOMENT 1 /* float_moment: 4 doubles per frame */
 #define VMX_FEATURE_PSNR 2   /* float_psnr: row sums and the MSE per frame */
@@ -165,8 +166,9 @@ int vmx_frames_ex(const void *ref, const void *dis, int width, int height, int64
                   void *workspace, size_t workspace_bytes, unsigned flags, void *stream);
 
 /*
- * Status of the last call that used `workspace`: VMX_OK, or VMX_ETIMEOUT if a
- * bounded device wait gave up. Synchronises `stream`.
+ * Status of the last call that used `workspace`: VMX_OK, VMX_ETIMEOUT if a
+ * bounded device wait gave up, or (a checked build only) VMX_ECHECK if an
+ * index check failed. Synchronises `stream`.
  */
 int vmx_workspace_status(const void *workspace, void *stream);
 
@@ -250,8 +252,9 @@ void vmx_frames_host_traffic(int width, int height, int64_t stride_bytes, int bp
  *               be NULL, and s2_rows, s2_sums, noise_sums may be NULL.
  *   outputs     device pointers, layout as vmx_moment_psnr_frames().
  *   status      device or NULL, one uint32: set on `stream` after the
- *               kernel to 0, or to 1 when a bounded device wait gave up (the
- *               outputs are then not valid).
+ *               kernel to 0, or to bit 0 when a bounded device wait gave up
+ *               and (a checked build only) bit 1 when an index check failed
+ *               (the outputs are then not valid).
  * Asynchronous on `stream`. Returns VMX_OK, VMX_EINVAL (arguments, as the
  * other calls), VMX_ESCRATCH, or VMX_ECUDA. Every argument is checked, and
  * VMX_EINVAL or VMX_ESCRATCH returned, before any CUDA call.
@@ -262,6 +265,22 @@ int vmx_frames_noalloc(const void *ref, const void *dis, int width, int height,
                        double *moments, uint64_t *s2_rows, uint64_t *s2_sums,
                        uint64_t *psnr_rows, double *mse, uint64_t *noise_sums,
                        uint32_t *status, void *stream);
+
+/*
+ * Checked builds (compiled with VMX_CHECK=1, a debug and test variant of the
+ * library): every index the kernels compute into one of their arrays is
+ * compared with the array's extent before the access; an index out of range
+ * skips the access and is reported, never trapped. No counterpart in the
+ * pages. vmx_checked_build() returns 1 in such a build, 0 otherwise. The
+ * frame kernel reports a failed check in its call's status (VMX_ECHECK from
+ * vmx_workspace_status() or a call with a NULL workspace); integer_psnr has
+ * no status word, so vmx_check_status() returns VMX_ECHECK if a check failed
+ * in any integer_psnr launch on the current device since the last call (and
+ * clears it), else VMX_OK; it synchronises `stream`. In other builds it
+ * returns VMX_OK at once.
+ */
+int vmx_checked_build(void);
+int vmx_check_status(void *stream);
 
 /* Name of a status code (and the last CUDA error for VMX_ECUDA). */
 const char *vmx_strerror(int status);

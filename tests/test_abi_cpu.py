@@ -35,10 +35,17 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_strerror(lib):
-    assert lib.vmx_version() == 10000
-    for code in (0, -1, -2, -3, -4):
-        assert lib.vmx_strerror(code)
+    assert lib.vmx_version() == 10100
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert lib.vmx_strerror(code) and lib.vmx_strerror(code) != b"unknown status"
     assert lib.vmx_strerror(-99) == b"unknown status"
+
+
+def test_default_build_is_not_checked(lib):
+    """The default library compiles its index checks to nothing: it says so,
+    and vmx_check_status has nothing to report (no CUDA call is made)."""
+    assert lib.vmx_checked_build() == 0
+    assert lib.vmx_check_status(None) == _lib.VMX_OK
 
 
 @pytest.mark.parametrize("args", [
