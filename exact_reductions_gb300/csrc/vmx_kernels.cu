@@ -212,6 +212,13 @@ __device__ __forceinline__ void bulk_to_smem(uint32_t dst, const void *src, uint
         : "memory");
 }
 
+// Asks `bytes` (a multiple of 16) from a 16-byte aligned global address into
+// L2, without waiting.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {
     uint4 v;
@@ -722,73 +729,126 @@ __device__ __forceinline__ void terms_of_word(uint32_t w, uint32_t *t0, uint32_t
     *t1 = p1 * p1 - (__float_as_uint(ei.y) - 0x4B400000u);
 }
 
-// The compact run of n consecutive terms under last place u = 2^sh (the
-// method of lane_run_fp in ordsum.cuh, with both start parities' binary32
-// trajectories advanced by one packed add). Valid while n * 2u < 2^22 (the
-// trajectory offsets stay exact small integers): n = 24 up to sh = 16.
+// A lane's binary32 trajectories under last place u = 2^sh (the method of
+// lane_run_fp in ordsum.cuh), both start parities advanced by one packed add
+// per term: after n terms, the compact run of those n terms. Exact while
+// n * 2u < 2^22 (the trajectory offsets stay exact small integers).
+struct Traj {
+    float2 F;
+    uint32_t tlo, vsum;
+};
+
+// The trajectories' start: 1.5 * 2^23 * u (even) and one place higher (odd).
+__device__ __forceinline__ float2 traj_start(int sh)
+{
+    const float uf = __uint_as_float((uint32_t)(127 + sh) << 23);  // 2^sh
+    const float f0e = __fmul_rn(12582912.0f, uf);
+    return make_float2(f0e, __fadd_rn(f0e, uf));
+}
+
 template <int N>
-__device__ __forceinline__ LaneRun lane_run_fp2(const uint32_t (&t)[N], int sh)
+__device__ __forceinline__ void traj_extend(Traj &T, const uint32_t (&t)[N], uint32_t vmask)
 {
     static_assert(N % 2 == 0, "terms come in pairs");
-    const float uf = __uint_as_float((uint32_t)(127 + sh) << 23);  // 2^sh
-    const float f0e = __fmul_rn(12582912.0f, uf);                // 1.5 * 2^23 * u
-    const float2 f0 = make_float2(f0e, __fadd_rn(f0e, uf));
-    float2 F = f0;
-    uint32_t tlo = 0, vsum = 0;
-    const uint32_t vmask = (2u << sh) - 1u;
     const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
 #pragma unroll
     for (int i = 0; i < N; i += 2) {
         const uint32_t v0 = t[i] & vmask, v1 = t[i + 1] & vmask;
-        tlo += t[i] + t[i + 1];
-        vsum += v0 + v1;
+        T.tlo += t[i] + t[i + 1];
+        T.vsum += v0 + v1;
         const float2 vf = __fadd2_rn(make_float2(__uint_as_float(v0 | kA), __uint_as_float(v1 | kA)), m23);
-        F = __fadd2_rn(F, make_float2(vf.x, vf.x));
-        F = __fadd2_rn(F, make_float2(vf.y, vf.y));
+        T.F = __fadd2_rn(T.F, make_float2(vf.x, vf.x));
+        T.F = __fadd2_rn(T.F, make_float2(vf.y, vf.y));
     }
-    const float2 dF = __fadd2_rn(F, make_float2(-f0.x, -f0.y));
+}
+
+__device__ __forceinline__ LaneRun traj_run(const Traj &T, float2 f0)
+{
+    const float2 dF = __fadd2_rn(T.F, make_float2(-f0.x, -f0.y));
     LaneRun r;
-    r.tlo = tlo;
-    r.d[0] = (int32_t)(__float_as_uint(__fadd_rn(dF.x, 12582912.0f)) - 0x4B400000u) - (int32_t)vsum;
-    r.d[1] = (int32_t)(__float_as_uint(__fadd_rn(dF.y, 12582912.0f)) - 0x4B400000u) - (int32_t)vsum;
+    r.tlo = T.tlo;
+    r.d[0] = (int32_t)(__float_as_uint(__fadd_rn(dF.x, 12582912.0f)) - 0x4B400000u) - (int32_t)T.vsum;
+    r.d[1] = (int32_t)(__float_as_uint(__fadd_rn(dF.y, 12582912.0f)) - 0x4B400000u) - (int32_t)T.vsum;
     return r;
 }
 
-// The run of a 16-bit row under binade e: passes of 32 lanes x 24 samples,
-// each lane's 24 consecutive terms a compact run, lanes composed by an
-// order-preserving shuffle tree (lane i takes lane i + off), passes composed
-// in order. Samples past the row are zero terms, which leave any run as it is.
+// The compact run of the N terms t (N = 24 is exact up to sh = 16).
+template <int N>
+__device__ __forceinline__ LaneRun lane_run_fp2(const uint32_t (&t)[N], int sh)
+{
+    const float2 f0 = traj_start(sh);
+    Traj T{f0, 0u, 0u};
+    traj_extend(T, t, (2u << sh) - 1u);
+    return traj_run(T, f0);
+}
+
+// Lanes' runs composed in lane order by a shuffle tree (lane i takes lane
+// i + off): every lane gets the run of all 32.
+__device__ __forceinline__ LaneRun warp_run_of_lanes(LaneRun l, int sh)
+{
+    const int lane = lane_id();
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        LaneRun o;
+        o.tlo = __shfl_down_sync(kFull, l.tlo, off);
+        o.d[0] = __shfl_down_sync(kFull, l.d[0], off);
+        o.d[1] = __shfl_down_sync(kFull, l.d[1], off);
+        if ((lane & (2 * off - 1)) == 0) l = lane_compose(l, o, sh);
+    }
+    LaneRun w;
+    w.tlo = __shfl_sync(kFull, l.tlo, 0);
+    w.d[0] = __shfl_sync(kFull, l.d[0], 0);
+    w.d[1] = __shfl_sync(kFull, l.d[1], 0);
+    return w;
+}
+
+// The run of a 16-bit row under binade e (so sh = e - 52 <= 10). In rounds
+// of at most 32 x 128 vectors, each lane takes a contiguous stretch of the
+// round (at most 1024 terms: 1024 * 2^11 < 2^22 keeps its trajectory exact
+// for every binade up to 62) and runs one trajectory through it; the lanes'
+// runs are composed in lane order, the rounds in row order. A lane reads its
+// stretch three vectors at a time, the next three already on their way.
+// Samples past the lane's stretch are zero terms, which leave a run as it is.
 template <bool VEC>
 __device__ __noinline__ Run row_run16(const unsigned char *row, int width, int e, uint64_t exact)
 {
-    constexpr int kRunVecs = 3;  // consecutive vectors per lane and pass
+    constexpr int kRunVecs = 3;     // vectors per lane and step
+    constexpr int kLaneVecs = 128;  // vectors per lane and round, at most
     const int lane = lane_id();
     const int sh = e - 52;
+    const uint32_t vmask = (2u << sh) - 1u;
+    const float2 f0 = traj_start(sh);
     const int nvt = (width + 7) >> 3;
     LaneRun acc = lane_identity();
-    for (int base = 0; base < nvt; base += 32 * kRunVecs) {
-        uint32_t t[8 * kRunVecs];
+    for (int base = 0; base < nvt; base += 32 * kLaneVecs) {
+        const int left = min(nvt - base, 32 * kLaneVecs);
+        const int per = (left + 31) >> 5;  // the round's vectors per lane
+        const int v0 = base + lane * per, v1 = min(base + left, v0 + per);
+        const auto load = [row, width, v1](int v) {
+            return v < v1 ? load_vec16_l1<VEC>(row, v, width) : make_uint4(0u, 0u, 0u, 0u);
+        };
+        Traj T{f0, 0u, 0u};
+        uint4 nx[kRunVecs];
 #pragma unroll
-        for (int u = 0; u < kRunVecs; ++u) {
-            const uint4 V = load_vec16_l1<VEC>(row, base + lane * kRunVecs + u, width);
-            const uint32_t w4[4] = {V.x, V.y, V.z, V.w};
+        for (int u = 0; u < kRunVecs; ++u) nx[u] = load(v0 + u);
+        for (int k = 0; k < per; k += kRunVecs) {
+            uint4 cv[kRunVecs];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) terms_of_word(w4[w], &t[8 * u + 2 * w], &t[8 * u + 2 * w + 1]);
+            for (int u = 0; u < kRunVecs; ++u) cv[u] = nx[u];
+            if (k + kRunVecs < per) {
+#pragma unroll
+                for (int u = 0; u < kRunVecs; ++u) nx[u] = load(v0 + k + kRunVecs + u);
+            }
+            uint32_t t[8 * kRunVecs];
+#pragma unroll
+            for (int u = 0; u < kRunVecs; ++u) {
+                const uint32_t w4[4] = {cv[u].x, cv[u].y, cv[u].z, cv[u].w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) terms_of_word(w4[w], &t[8 * u + 2 * w], &t[8 * u + 2 * w + 1]);
+            }
+            traj_extend(T, t, vmask);
         }
-        LaneRun l = lane_run_fp2(t, sh);
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            LaneRun o;
-            o.tlo = __shfl_down_sync(kFull, l.tlo, off);
-            o.d[0] = __shfl_down_sync(kFull, l.d[0], off);
-            o.d[1] = __shfl_down_sync(kFull, l.d[1], off);
-            if ((lane & (2 * off - 1)) == 0) l = lane_compose(l, o, sh);
-        }
-        LaneRun seg;
-        seg.tlo = __shfl_sync(kFull, l.tlo, 0);
-        seg.d[0] = __shfl_sync(kFull, l.d[0], 0);
-        seg.d[1] = __shfl_sync(kFull, l.d[1], 0);
-        acc = lane_compose(acc, seg, sh);
+        acc = lane_compose(acc, warp_run_of_lanes(traj_run(T, f0), sh), sh);
     }
     return lane_to_run(acc, exact);
 }
@@ -1703,6 +1763,103 @@ __device__ __noinline__ void lookback(const Params &p, int f, int j, uint64_t ag
     *pre_d = pd;
 }
 
+// Phase B of item j of frame f (rows [r0, r1), lane i holding row r0 + i's
+// exact sums my_r, my_d; aggr, aggd the item's): the exact sums before the
+// item by the look-back, each row's plan from its exact prefix, and the run
+// of every row planned from binade 55 up (its record, else a record of no
+// run). A function of its own, so that its state holds no registers in the
+// row loop.
+template <bool VEC>
+__device__ __noinline__ void plan_and_runs(const Params &p, int f, int j, int r0, int r1, uint64_t my_r,
+                                           uint64_t my_d, uint64_t aggr, uint64_t aggd)
+{
+    const int lane = lane_id(), H = p.height;
+    uint64_t pr = 0, pd = 0;
+    lookback(p, f, j, aggr, aggd, &pr, &pd);
+    // Lane i plans row r0 + i of both planes from the row's exact prefix.
+    SC tot;
+    const uint64_t exr = warp_excl_sc(SC{my_r, 0}, &tot).s;
+    const uint64_t exd = warp_excl_sc(SC{my_d, 0}, &tot).s;
+    const bool mine = lane < r1 - r0;
+    const int er = mine ? plan_binade(pr + exr, my_r) : 0;
+    const int ed = mine ? plan_binade(pd + exd, my_d) : 0;
+    // The rows to run are read a second time, one after another: all of
+    // them are asked into L2 at once, so that only the first waits on DRAM.
+    const uint32_t bytes = ((uint32_t)p.width * 2u) & ~15u;
+    if (VEC && bytes > 0u && mine && chk(p.status, (size_t)f * H + r0 + lane, ext_frame_rows(p))) {
+        const int64_t off = (int64_t)f * p.pitch + (int64_t)(r0 + lane) * p.stride;
+        if (er >= 55) prefetch_l2(p.ref + off, bytes);
+        if (ed >= 55) prefetch_l2(p.dis + off, bytes);
+    }
+    for (int X = 0; X < 2; ++X) {
+        const unsigned char *plane = (X ? p.dis : p.ref) + (int64_t)f * p.pitch;
+        for (int r = r0; r < r1; ++r) {
+            const int li = r - r0;
+            const int e = __shfl_sync(kFull, X ? ed : er, li);
+            RowRec rec = {0ull, 0, 0, kRowNone, 0};
+            if (e >= 55) {
+                const uint64_t rs = __shfl_sync(kFull, X ? my_d : my_r, li);
+                const Run run = row_run16<VEC>(plane + (int64_t)r * p.stride, p.width, e, rs);
+                rec.inc0 = run.inc[0];
+                rec.dinc = (int32_t)(run.inc[1] - run.inc[0]);
+                rec.e = (uint8_t)e;
+                rec.kind = kRowRun;
+            }
+            const size_t k = ((size_t)f * 2 + X) * H + r;
+            if (lane == 0 && chk(p.status, k, ext_plane_rows(p))) p.rec[k] = rec;
+        }
+    }
+}
+
+// C. completion of item j of frame f: the item counts itself in its block
+// (32-bit), one release per item (its records, then its count); the block's
+// last item to finish acquires them all (with one fence unless the count
+// was taken acquire-release) and writes the block's record. (A test of the
+// bounded waits asks for one item more than a block holds: no block
+// completes.) Called by the whole warp.
+template <bool FULL>
+__device__ __forceinline__ void complete_item(const Params &p, int f, int j)
+{
+    const int b = j / kBlockItems, NB = p.blocks_per_frame;
+    uint32_t last = 0;
+    if (lane_id() == 0) {
+        uint32_t *cnt = p.block_fin + (size_t)f * NB + b;
+        const uint32_t old = !chk(p.status, (size_t)f * NB + b, ext_blocks(p)) ? 0u
+                             : FULL ? atom_add_acq_rel(cnt, 1u)
+                                    : atom_add_release(cnt, 1u);
+        last = old + 1u == block_items(p, b) + p.test_stall ? 1u : 0u;
+        if (last && !FULL) fence_acq_rel();
+    }
+    if (__shfl_sync(kFull, last, 0)) {
+        __syncwarp();  // lane 0's acquire before the other lanes' reads
+        fold_block(p, f, b);
+    }
+}
+
+// A streamed item whose plan is still to come: its frame and index, its
+// exact sums, and each row's (lane i's row r0 + i).
+struct ParkSlot {
+    uint64_t rows[2][kMaxRowsPerItem];
+    uint64_t agg[2];
+    int f, j;
+};
+
+// Phases B and C of the item in a warp's slot. Called by the whole warp.
+template <bool VEC, bool FULL>
+__device__ __noinline__ void resume_parked(const Params &p, const ParkSlot &q)
+{
+    const int lane = lane_id();
+    const int f = q.f, j = q.j;
+    const int r0 = j * p.rows_per_item, r1 = min(p.height, r0 + p.rows_per_item);
+    uint64_t my_r = 0, my_d = 0;
+    if (lane < r1 - r0) {
+        my_r = q.rows[0][lane];
+        my_d = q.rows[1][lane];
+    }
+    plan_and_runs<VEC>(p, f, j, r0, r1, my_r, my_d, q.agg[0], q.agg[1]);
+    complete_item<FULL>(p, f, j);
+}
+
 // The order items are handed out in: frame by frame, except that the last
 // kTailFrames frames (all of them in a batch of at most that many) go row by
 // row across those frames. A frame's crossing row (about three quarters down
@@ -1730,7 +1887,7 @@ template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC, bool LOW>
 __global__ void __maxnreg__(kMaxRegs) frames_kernel(Params p)
 {
     const int lane = lane_id();
-    const int I = p.items_per_frame, NB = p.blocks_per_frame;
+    const int I = p.items_per_frame;
     const int nitems = p.frames * I;
     const int H = p.height;
     // Items are handed out by a ticket counter only, in chunks of
@@ -1743,6 +1900,8 @@ __global__ void __maxnreg__(kMaxRegs) frames_kernel(Params p)
     // deadlock-free: a warp works through its chunk in order, so the
     // smallest unfinished item is always some running warp's current item.
     __shared__ RowSlot item_rows[kWarps][kMaxRowsPerItem];  // sums of an item's rows
+    __shared__ ParkSlot park[FULL && M ? kWarps : 1];         // an item waiting for its plan
+    bool parked = false;
     const int wid = (int)(threadIdx.x >> 5);
     // 16-bit rows on 16-byte boundaries stream through shared memory.
     constexpr bool STG = kStages > 0 && VEC && sizeof(TS) == 2;
@@ -1851,57 +2010,32 @@ __global__ void __maxnreg__(kMaxRegs) frames_kernel(Params p)
         }
 
         // B. frames that can pass 2^55: runs of the rows planned from 55 up.
+        // An item's plan waits for every item of the frame before it, so it
+        // is taken up only after the warp has streamed its next item (the
+        // item parked meanwhile in the warp's shared slot): by then those
+        // items are out, and the warp seldom waits.
         if (FULL && M) {
-            uint64_t pr = 0, pd = 0;
-            lookback(p, f, j, g.s2[0], g.s2[1], &pr, &pd);
-            for (int X = 0; X < 2; ++X) {
-                const uint64_t pre = X ? pd : pr;
-                const uint64_t mine = X ? my_d : my_r;
-                SC tot;
-                const uint64_t ex = warp_excl_sc(SC{mine, 0}, &tot).s;
-                const unsigned char *plane = X ? fd : fr;
-                for (int r = r0; r < r1; ++r) {
-                    const int li = r - r0;
-                    const uint64_t rp = pre + __shfl_sync(kFull, ex, li);
-                    const uint64_t rs = __shfl_sync(kFull, mine, li);
-                    const int e = plan_binade(rp, rs);
-                    RowRec rec = {0ull, 0, 0, kRowNone, 0};
-                    if (e >= 55) {
-                        const Run run = row_run16<VEC>(plane + (int64_t)r * p.stride, p.width, e, rs);
-                        rec.inc0 = run.inc[0];
-                        rec.dinc = (int32_t)(run.inc[1] - run.inc[0]);
-                        rec.e = (uint8_t)e;
-                        rec.kind = kRowRun;
-                    }
-                    const size_t k = ((size_t)f * 2 + X) * H + r;
-                    if (lane == 0 && chk(p.status, k, ext_plane_rows(p))) p.rec[k] = rec;
-                }
+            if (parked) resume_parked<VEC, FULL>(p, park[wid]);
+            __syncwarp();
+            if (lane < r1 - r0) {
+                park[wid].rows[0][lane] = my_r;
+                park[wid].rows[1][lane] = my_d;
             }
+            if (lane == 0) {
+                park[wid].agg[0] = g.s2[0];
+                park[wid].agg[1] = g.s2[1];
+                park[wid].f = f;
+                park[wid].j = j;
+            }
+            __syncwarp();
+            parked = true;
+            continue;
         }
 
-        // C. completion: the item counts itself in its block (32-bit); the
-        // block's last item to finish writes the block's record. (A test of
-        // the bounded waits asks for one item more than a block holds: no
-        // block completes.)
-        {
-            // One release per item (its records, then its count); the last
-            // item of the block acquires them all with one fence.
-            const int b = j / kBlockItems;
-            uint32_t last = 0;
-            if (lane == 0) {
-                uint32_t *cnt = p.block_fin + (size_t)f * NB + b;
-                const uint32_t old = !chk(p.status, (size_t)f * NB + b, ext_blocks(p)) ? 0u
-                                     : FULL ? atom_add_acq_rel(cnt, 1u)
-                                            : atom_add_release(cnt, 1u);
-                last = old + 1u == block_items(p, b) + p.test_stall ? 1u : 0u;
-                if (last && !FULL) fence_acq_rel();
-            }
-            if (__shfl_sync(kFull, last, 0)) {
-                __syncwarp();  // lane 0's acquire before the other lanes' reads
-                fold_block(p, f, b);
-            }
-        }
+        // C. completion.
+        complete_item<FULL>(p, f, j);
     }
+    if (FULL && M && parked) resume_parked<VEC, FULL>(p, park[wid]);
 
     // Every chunk a warp started it has read, unless a wait gave up: then
     // wait (bounded) for the copies still landing in its buffers.
