@@ -12,23 +12,29 @@
 namespace vmx {
 
 #ifndef VMX_THREADS
-#define VMX_THREADS 128
+#define VMX_THREADS 32
 #endif
-// Threads per CTA: four independent warps; six CTAs per SM (see
-// kMaxRegs). Small CTAs free their slots early when the items run out, for
-// the next call's kernel.
+// Threads per CTA: one warp (the warps share nothing but a CTA's slot), so
+// that the register cap alone sets the warps per SM (28 at kMaxRegs; four-
+// warp CTAs at 80 registers held 24), and a warp that runs out of items
+// frees its slot for the next call's kernel at once.
 constexpr int kThreads = VMX_THREADS;
 constexpr int kWarps = kThreads / 32;
 #ifndef VMX_MAX_REGS
-#define VMX_MAX_REGS 80
+#define VMX_MAX_REGS 72
+#endif
+#ifndef VMX_MAX_REGS_FULL
+#define VMX_MAX_REGS_FULL 80
 #endif
 #ifndef VMX_UNROLL
 #define VMX_UNROLL 3
 #endif
-// Registers per thread of the frame kernel, at most: 80 keeps six CTAs of
-// 128 threads on an SM (registers go out 256 a warp). A cap, rather than
-// launch bounds asking for six CTAs, measured faster at the same count.
+// Registers per thread of the frame kernel, at most (registers go out 256 a
+// warp): 72 keeps 28 one-warp CTAs on an SM; 80, 25, for the instances with
+// the look-back, whose phase B spills more under 72. A cap, rather than
+// launch bounds asking for a CTA count, measured faster at the same count.
 constexpr int kMaxRegs = VMX_MAX_REGS;
+constexpr int kMaxRegsFull = VMX_MAX_REGS_FULL;
 constexpr int kMaxRowsPerItem = 32;        // rows per item, at most
 #ifndef VMX_MAX_CHUNK
 #define VMX_MAX_CHUNK 4

@@ -1884,7 +1884,7 @@ __device__ __forceinline__ void item_of_ticket(int tk, int F, int I, int *f, int
 }
 
 template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC, bool LOW>
-__global__ void __maxnreg__(kMaxRegs) frames_kernel(Params p)
+__global__ void __maxnreg__(FULL ? kMaxRegsFull : kMaxRegs) frames_kernel(Params p)
 {
     const int lane = lane_id();
     const int I = p.items_per_frame;
