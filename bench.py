@@ -479,6 +479,39 @@ def run_ours(args, rank, local_rank, world, pg):
         raise SystemExit("bench: the timed outputs differ from the oracle")
 
 
+def phase_split(R, D, bpc):
+    """Where one call's time goes, from the timing build of the library
+    (VMX_PHASE_TIMES=1, vmx_phase_times): warp-microseconds per phase summed
+    over the warps (SM cycles at the device's clock rate), and when the warps
+    ran out of items and the walks ended, from the first warp's start."""
+    import torch
+
+    from exact_reductions_gb300 import _lib, api, build
+
+    with _lib.using(build.build_variant("phase_times", ["VMX_PHASE_TIMES=1"])) as lib:
+        out = api.frames(R, D, bpc, features=3)  # the first call allocates
+        torch.cuda.synchronize()
+        _lib.check(lib.vmx_phase_times(None, 1), "phase times")
+        api.frames(R, D, bpc, features=3, ws=out["_workspace"])
+        torch.cuda.synchronize()
+        c = np.zeros(16, dtype=np.uint64)
+        _lib.check(lib.vmx_phase_times(c.ctypes.data, 1), "phase times")
+    c = [int(x) for x in c]
+    mhz = c[15] / 1e3
+    t0 = c[0]
+    return {
+        "span_us": (c[1] - t0) / 1e3,
+        "first_warp_out_of_items_us": (c[7] - t0) / 1e3,
+        "last_warp_out_of_items_us": (c[6] - t0) / 1e3,
+        "last_walk_end_us": (c[9] - t0) / 1e3 if c[10] else None,
+        "warp_us": {"streaming": c[2] / mhz, "look_back": c[3] / mhz, "plans_and_runs": c[4] / mhz,
+                    "completion": c[5] / mhz, "walks": c[8] / mhz},
+        "items": c[11], "row_runs": c[14], "walks": c[10],
+        "longest_walk_us": c[12] / mhz,
+        "clock_note": f"cycles at the device's {mhz:.0f} MHz clock rate",
+    }
+
+
 def run_configs(args):
     """One JSON line per workload (C1..C5c): GPU frames/s and GB/s with
     inputs resident (calls one at a time, and as a stream of batches), the
@@ -495,9 +528,12 @@ def run_configs(args):
     dev = torch.device("cuda", 0)
     peak, peak_kind = peak_hbm()
     threads = os.cpu_count() or 1
-    for key in ("C1", "C2", "C3", "C4", "C5a", "C5b", "C5c"):
+    keys = ("C1", "C2", "C3", "C4", "C5a", "C5b", "C5c")
+    if args.only:
+        keys = [k for k in keys if k in args.only.split(",")]
+    for key in keys:
         wl = synth.WORKLOADS[key]
-        ref, dis = wl.batch()
+        ref, dis = wl.batch(args.frames) if args.frames > 0 else wl.batch()
         F = ref.shape[0]
         R = torch.from_numpy(ref).to(dev)
         D = torch.from_numpy(dis).to(dev)
@@ -515,6 +551,8 @@ def run_configs(args):
         torch.cuda.synchronize()
         t = s.elapsed_time(e) / 1e3 / reps
         status = api.workspace_status(ws)
+        walk = [int(x) for x in api.workspace_stats(ws)]  # the last call's walks
+        split = phase_split(R, D, wl.bpc) if args.phase_times else None
         # The same calls as a stream of batches: graphs of sixteen calls,
         # each kernel overlapping the one before (the bench's mode).
         fg = api.FrameGraph(R, D, wl.bpc, features=3, depth=16)
@@ -551,7 +589,10 @@ def run_configs(args):
             "stream_frames_per_s": F / tg, "stream_frac_of_peak": F * wl.frame_pair_bytes / tg / 1e9 / peak,
             "oracle_ms_per_frame_1core": one_core * 1e3,
             "oracle_frames_per_s_all_cores": all_cores, "oracle_cores": min(threads, n),
-            "bit_exact_frames_checked": n, "bit_exact": exact and status == 0}), flush=True)
+            "bit_exact_frames_checked": n, "bit_exact": exact and status == 0,
+            "walk_rows": {"exact": walk[0], "closed_form_or_run": walk[1], "by_terms": walk[2],
+                          "search_passes": walk[3]},
+            **({"phase_times": split} if split else {})}), flush=True)
         del R, D, out, ws
         torch.cuda.empty_cache()
 
@@ -565,6 +606,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--configs", action="store_true",
                     help="one line per workload C1..C5c (GPU, oracle, bit-exactness) instead")
+    ap.add_argument("--only", default="",
+                    help="with --configs: these workloads only (comma-separated, e.g. C4,C5c)")
+    ap.add_argument("--frames", type=int, default=0,
+                    help="with --configs: frame pairs per call instead of each workload's own")
+    ap.add_argument("--phase-times", action="store_true",
+                    help="with --configs: add where one call's warp time goes (a timing build)")
     args = ap.parse_args()
     if args.configs:
         run_configs(args)

@@ -8,6 +8,7 @@ kernels.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -54,6 +55,7 @@ SIGNATURES = {
                                   _vp, _vp, _vp, _vp, _vp]),
     "vmx_checked_build": (_i32, []),
     "vmx_check_status": (_i32, [_vp]),
+    "vmx_phase_times": (_i32, [_vp, _i32]),
     "vmx_strerror": (ctypes.c_char_p, [_i32]),
     "vmx_kernel_launches": (_u64, []),
     "vmx_version": (_i32, []),
@@ -88,6 +90,19 @@ def load() -> ctypes.CDLL:
             "`python -c 'import __graft_entry__ as g; g.build()'` first")
     _lib = bind(path)
     return _lib
+
+
+@contextlib.contextmanager
+def using(path: str):
+    """Run the enclosed calls on the libvmx build at `path` (a variant such as
+    a timing or checked build), then go back to the default library."""
+    global _lib
+    old = _lib
+    _lib = bind(path)
+    try:
+        yield _lib
+    finally:
+        _lib = old
 
 
 class VmxError(RuntimeError):

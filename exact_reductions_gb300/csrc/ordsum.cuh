@@ -197,8 +197,9 @@ VMX_HD uint32_t term_of_diff(uint32_t a, uint32_t b)
     return term_of_sample(a > b ? a - b : b - a);
 }
 
-// A lane's run of up to eight consecutive terms, in compact form: the sum of
-// the terms modulo 2^32 (enough for parities, since 2u divides 2^32) and, for
+// A lane's run of consecutive terms, in compact form: a number congruent to
+// the terms' sum modulo 2u (all that composing and the parities read; the
+// CPU model keeps the sum modulo 2^32, the device the residues' sum) and, for
 // each start parity, the run's increment minus the exact sum of its terms (a
 // small signed number).
 struct LaneRun {

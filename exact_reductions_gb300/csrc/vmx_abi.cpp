@@ -244,9 +244,16 @@ using namespace vmx;
 
 extern "C" {
 
-int vmx_version(void) { return 10100; }
+int vmx_version(void) { return 10200; }
 
 int vmx_checked_build(void) { return VMX_CHECK ? 1 : 0; }
+
+int vmx_phase_times(uint64_t *out, int reset)
+{
+    if (!VMX_PHASE_TIMES || (!out && !reset)) return VMX_EINVAL;
+    const cudaError_t err = phase_times(out, reset != 0);
+    return err == cudaSuccess ? VMX_OK : cuda_fail(err);
+}
 
 int vmx_check_status(void *stream)
 {

@@ -72,6 +72,32 @@ constexpr uint32_t kPipeSpinLimit = 1u << 20;  // polls of one chunk's barrier, 
 #define VMX_FIRST_UNROLL 16
 #endif
 constexpr int kFirstUnroll = VMX_FIRST_UNROLL;  // loads in flight per lane in the walks' sequential sums
+// Timing builds (VMX_PHASE_TIMES=1, a profiling variant of the library):
+// the frame kernel sums each phase's clock cycles over its warps and stamps
+// a few events with the global timer, into counters vmx_phase_times() reads.
+#ifndef VMX_PHASE_TIMES
+#define VMX_PHASE_TIMES 0
+#endif
+enum PhaseCounter : int {
+    kPtStart = 0,       // first warp's start (global timer, ns)
+    kPtEnd = 1,         // last warp's end (ns)
+    kPtStream = 2,      // phase A: items streamed (cycles, summed over warps)
+    kPtLookback = 3,    // phase B: look-back, waits included (cycles)
+    kPtRuns = 4,        // phase B: plans and row runs (cycles)
+    kPtComplete = 5,    // phase C: completion (cycles)
+    kPtOutLast = 6,     // last warp out of items (ns)
+    kPtOutFirst = 7,    // first warp out of items (ns)
+    kPtWalks = 8,       // phase D: walks, waits included (cycles)
+    kPtWalksEnd = 9,    // last walk's end (ns)
+    kPtWalkTasks = 10,  // walks taken
+    kPtItems = 11,      // items streamed
+    kPtWalkMax = 12,    // longest walk (cycles)
+    kPtWalksStart = 13, // first walk's start (ns)
+    kPtRunRows = 14,    // row runs formed in phase B
+    kPtClockKHz = 15,   // the device's SM clock rate (kHz; filled by the reader)
+    kPtCount = 16
+};
+
 #ifndef VMX_CHECK
 // 1: a checked build (a test variant). Every index the kernels compute into
 // one of their arrays is compared with the array's extent first; one out of
@@ -162,6 +188,10 @@ struct Params {
 // every row starts on a 16-byte boundary.
 cudaError_t launch_frames(const Params &p, const Layout &L, int features, bool vec,
                           cudaStream_t stream);
+
+// A timing build's counters (kPtCount) of the current device into `out`
+// (when not null), then, when `reset`, cleared for the next launches.
+cudaError_t phase_times(uint64_t *out, bool reset);
 
 // Device address of the current device's static scratch array of
 // VMX_NOALLOC_SCRATCH_BYTES bytes (cudaGetSymbolAddress; no allocation).

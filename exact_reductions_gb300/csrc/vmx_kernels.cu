@@ -107,6 +107,38 @@ __device__ __forceinline__ bool chk(uint32_t *status, size_t i, size_t n)
 __device__ __forceinline__ bool chk(uint32_t *, size_t, size_t) { return true; }
 #endif
 
+// Timing-build counters (PhaseCounter): lane 0 of a warp adds or stamps.
+__device__ unsigned long long g_phase[kPtCount];
+#if VMX_PHASE_TIMES
+__device__ __forceinline__ unsigned long long pt_now()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ long long pt_clock() { return clock64(); }
+__device__ __forceinline__ void pt_add(int k, unsigned long long v)
+{
+    if ((threadIdx.x & 31u) == 0u) atomicAdd(&g_phase[k], v);
+}
+__device__ __forceinline__ void pt_cycles(int k, long long since) { pt_add(k, (unsigned long long)(clock64() - since)); }
+__device__ __forceinline__ void pt_max(int k, unsigned long long v)
+{
+    if ((threadIdx.x & 31u) == 0u) atomicMax(&g_phase[k], v);
+}
+__device__ __forceinline__ void pt_min(int k, unsigned long long v)
+{
+    if ((threadIdx.x & 31u) == 0u) atomicMin(&g_phase[k], v);
+}
+#else
+__device__ __forceinline__ unsigned long long pt_now() { return 0ull; }
+__device__ __forceinline__ long long pt_clock() { return 0ll; }
+__device__ __forceinline__ void pt_add(int, unsigned long long) {}
+__device__ __forceinline__ void pt_cycles(int, long long) {}
+__device__ __forceinline__ void pt_max(int, unsigned long long) {}
+__device__ __forceinline__ void pt_min(int, unsigned long long) {}
+#endif
+
 // Extents (elements) of the kernel's arrays; a test of a checked build takes
 // the per-plane row arrays' as one less, so that a check fires.
 __device__ __forceinline__ size_t ext_plane_rows(const Params &p)
@@ -732,10 +764,14 @@ __device__ __forceinline__ void terms_of_word(uint32_t w, uint32_t *t0, uint32_t
 // A lane's binary32 trajectories under last place u = 2^sh (the method of
 // lane_run_fp in ordsum.cuh), both start parities advanced by one packed add
 // per term: after n terms, the compact run of those n terms. Exact while
-// n * 2u < 2^22 (the trajectory offsets stay exact small integers).
+// n * 2u < 2^22 (the trajectory offsets stay exact small integers). Only a
+// term's residue v = t mod 2u matters for its rounding, and the run's parity
+// needs the terms' sum only modulo 2u, which the residues' sum gives: each
+// residue is kept as the bits of the binary32 2^23 + v (one three-input
+// logic op), whose integer sum carries v's sum in its low 24 bits.
 struct Traj {
     float2 F;
-    uint32_t tlo, vsum;
+    uint32_t gsum;  // sum of the residues' binary32 bits: low 24 bits the residues' sum
 };
 
 // The trajectories' start: 1.5 * 2^23 * u (even) and one place higher (odd).
@@ -753,22 +789,24 @@ __device__ __forceinline__ void traj_extend(Traj &T, const uint32_t (&t)[N], uin
     const float2 m23 = make_float2(-8388608.0f, -8388608.0f);
 #pragma unroll
     for (int i = 0; i < N; i += 2) {
-        const uint32_t v0 = t[i] & vmask, v1 = t[i + 1] & vmask;
-        T.tlo += t[i] + t[i + 1];
-        T.vsum += v0 + v1;
-        const float2 vf = __fadd2_rn(make_float2(__uint_as_float(v0 | kA), __uint_as_float(v1 | kA)), m23);
+        const uint32_t g0 = (t[i] & vmask) | kA, g1 = (t[i + 1] & vmask) | kA;
+        T.gsum += g0 + g1;
+        const float2 vf = __fadd2_rn(make_float2(__uint_as_float(g0), __uint_as_float(g1)), m23);
         T.F = __fadd2_rn(T.F, make_float2(vf.x, vf.x));
         T.F = __fadd2_rn(T.F, make_float2(vf.y, vf.y));
     }
 }
 
+// The compact run: tlo the terms' sum modulo 2u (all that composing and the
+// parities read of it), d each parity's increment less the terms' sum.
 __device__ __forceinline__ LaneRun traj_run(const Traj &T, float2 f0)
 {
     const float2 dF = __fadd2_rn(T.F, make_float2(-f0.x, -f0.y));
+    const int32_t vsum = (int32_t)(T.gsum & 0xFFFFFFu);  // below 2^22
     LaneRun r;
-    r.tlo = T.tlo;
-    r.d[0] = (int32_t)(__float_as_uint(__fadd_rn(dF.x, 12582912.0f)) - 0x4B400000u) - (int32_t)T.vsum;
-    r.d[1] = (int32_t)(__float_as_uint(__fadd_rn(dF.y, 12582912.0f)) - 0x4B400000u) - (int32_t)T.vsum;
+    r.tlo = (uint32_t)vsum;
+    r.d[0] = (int32_t)(__float_as_uint(__fadd_rn(dF.x, 12582912.0f)) - 0x4B400000u) - vsum;
+    r.d[1] = (int32_t)(__float_as_uint(__fadd_rn(dF.y, 12582912.0f)) - 0x4B400000u) - vsum;
     return r;
 }
 
@@ -777,7 +815,7 @@ template <int N>
 __device__ __forceinline__ LaneRun lane_run_fp2(const uint32_t (&t)[N], int sh)
 {
     const float2 f0 = traj_start(sh);
-    Traj T{f0, 0u, 0u};
+    Traj T{f0, 0u};
     traj_extend(T, t, (2u << sh) - 1u);
     return traj_run(T, f0);
 }
@@ -810,7 +848,7 @@ __device__ __forceinline__ LaneRun warp_run_of_lanes(LaneRun l, int sh)
 // stretch three vectors at a time, the next three already on their way.
 // Samples past the lane's stretch are zero terms, which leave a run as it is.
 template <bool VEC>
-__device__ __noinline__ Run row_run16(const unsigned char *row, int width, int e, uint64_t exact)
+__device__ __forceinline__ Run row_run16(const unsigned char *row, int width, int e, uint64_t exact)
 {
     constexpr int kRunVecs = 3;     // vectors per lane and step
     constexpr int kLaneVecs = 128;  // vectors per lane and round, at most
@@ -827,7 +865,7 @@ __device__ __noinline__ Run row_run16(const unsigned char *row, int width, int e
         const auto load = [row, width, v1](int v) {
             return v < v1 ? load_vec16_l1<VEC>(row, v, width) : make_uint4(0u, 0u, 0u, 0u);
         };
-        Traj T{f0, 0u, 0u};
+        Traj T{f0, 0u};
         uint4 nx[kRunVecs];
 #pragma unroll
         for (int u = 0; u < kRunVecs; ++u) nx[u] = load(v0 + u);
@@ -1775,7 +1813,10 @@ __device__ __noinline__ void plan_and_runs(const Params &p, int f, int j, int r0
 {
     const int lane = lane_id(), H = p.height;
     uint64_t pr = 0, pd = 0;
+    const long long t0 = pt_clock();
     lookback(p, f, j, aggr, aggd, &pr, &pd);
+    const long long t1 = pt_clock();
+    pt_add(kPtLookback, (unsigned long long)(t1 - t0));
     // Lane i plans row r0 + i of both planes from the row's exact prefix.
     SC tot;
     const uint64_t exr = warp_excl_sc(SC{my_r, 0}, &tot).s;
@@ -1800,6 +1841,7 @@ __device__ __noinline__ void plan_and_runs(const Params &p, int f, int j, int r0
             if (e >= 55) {
                 const uint64_t rs = __shfl_sync(kFull, X ? my_d : my_r, li);
                 const Run run = row_run16<VEC>(plane + (int64_t)r * p.stride, p.width, e, rs);
+                pt_add(kPtRunRows, 1ull);
                 rec.inc0 = run.inc[0];
                 rec.dinc = (int32_t)(run.inc[1] - run.inc[0]);
                 rec.e = (uint8_t)e;
@@ -1809,6 +1851,7 @@ __device__ __noinline__ void plan_and_runs(const Params &p, int f, int j, int r0
             if (lane == 0 && chk(p.status, k, ext_plane_rows(p))) p.rec[k] = rec;
         }
     }
+    pt_cycles(kPtRuns, t1);
 }
 
 // C. completion of item j of frame f: the item counts itself in its block
@@ -1820,6 +1863,7 @@ __device__ __noinline__ void plan_and_runs(const Params &p, int f, int j, int r0
 template <bool FULL>
 __device__ __forceinline__ void complete_item(const Params &p, int f, int j)
 {
+    const long long t0 = pt_clock();
     const int b = j / kBlockItems, NB = p.blocks_per_frame;
     uint32_t last = 0;
     if (lane_id() == 0) {
@@ -1834,6 +1878,7 @@ __device__ __forceinline__ void complete_item(const Params &p, int f, int j)
         __syncwarp();  // lane 0's acquire before the other lanes' reads
         fold_block(p, f, b);
     }
+    pt_cycles(kPtComplete, t0);
 }
 
 // A streamed item whose plan is still to come: its frame and index, its
@@ -1923,6 +1968,7 @@ __global__ void __maxnreg__(FULL ? kMaxRegsFull : kMaxRegs) frames_kernel(Params
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t nwarps = gridDim.x * (uint32_t)kWarps;
     uint32_t cur = 0u, end = 0u, seen = 0u;
+    pt_min(kPtStart, pt_now());
     for (;;) {
         if (cur >= end) {
             const uint32_t left = (uint32_t)nitems > seen ? (uint32_t)nitems - seen : 0u;
@@ -1938,6 +1984,7 @@ __global__ void __maxnreg__(FULL ? kMaxRegsFull : kMaxRegs) frames_kernel(Params
         if (tk >= nitems) break;
         int f, j;
         item_of_ticket(tk, p.frames, I, &f, &j);
+        const long long ta = pt_clock();
         const int r0 = j * p.rows_per_item, r1 = min(H, r0 + p.rows_per_item);
         const unsigned char *fr = p.ref + (int64_t)f * p.pitch;
         const unsigned char *fd = p.dis + (int64_t)f * p.pitch;
@@ -2009,6 +2056,8 @@ __global__ void __maxnreg__(FULL ? kMaxRegsFull : kMaxRegs) frames_kernel(Params
             if (FULL) st_release(p.flags + (size_t)f * I + j, 1u);
         }
 
+        pt_cycles(kPtStream, ta);
+        pt_add(kPtItems, 1ull);
         // B. frames that can pass 2^55: runs of the rows planned from 55 up.
         // An item's plan waits for every item of the frame before it, so it
         // is taken up only after the warp has streamed its next item (the
@@ -2036,6 +2085,8 @@ __global__ void __maxnreg__(FULL ? kMaxRegsFull : kMaxRegs) frames_kernel(Params
         complete_item<FULL>(p, f, j);
     }
     if (FULL && M && parked) resume_parked<VEC, FULL>(p, park[wid]);
+    pt_max(kPtOutLast, pt_now());
+    pt_min(kPtOutFirst, pt_now());
 
     // Every chunk a warp started it has read, unless a wait gave up: then
     // wait (bounded) for the copies still landing in its buffers.
@@ -2056,11 +2107,18 @@ __global__ void __maxnreg__(FULL ? kMaxRegsFull : kMaxRegs) frames_kernel(Params
         wt = __shfl_sync(kFull, wt, 0);
         if (wt >= p.frames * kParts) break;
         const int wf = wt / kParts, part = wt - wf * kParts;
+        const long long tw = pt_clock();
+        pt_min(kPtWalksStart, pt_now());
         walk_part<TS, M, P, ODD, FULL, VEC>(p, wf, M ? part : 2);
+        pt_cycles(kPtWalks, tw);
+        pt_max(kPtWalkMax, (unsigned long long)(pt_clock() - tw));
+        pt_add(kPtWalkTasks, 1ull);
+        pt_max(kPtWalksEnd, pt_now());
     }
     // Launched to overlap the previous kernel: finish after it, so that the
     // stream's later work still follows both.
     if (p.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
+    pt_max(kPtEnd, pt_now());
 }
 
 template <typename TS, bool M, bool P, bool ODD, bool FULL, bool VEC, bool LOW>
@@ -2151,6 +2209,23 @@ cudaError_t launch_frames(const Params &p, const Layout &L, int features, bool v
 // Scratch of vmx_frames_noalloc: a fixed array in the module's static device
 // memory, one per device, 256-byte aligned like a caller's workspace.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[VMX_NOALLOC_SCRATCH_BYTES];
+
+cudaError_t phase_times(uint64_t *out, bool reset)
+{
+    if (out) {
+        cudaError_t err = cudaMemcpyFromSymbol(out, g_phase, sizeof(g_phase));
+        if (err != cudaSuccess) return err;
+        int dev = 0, khz = 0;
+        err = cudaGetDevice(&dev);
+        if (err == cudaSuccess) err = cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev);
+        if (err != cudaSuccess) return err;
+        out[kPtClockKHz] = (uint64_t)khz;
+    }
+    if (!reset) return cudaSuccess;
+    unsigned long long z[kPtCount] = {0};
+    z[kPtStart] = z[kPtOutFirst] = z[kPtWalksStart] = ~0ull;
+    return cudaMemcpyToSymbol(g_phase, z, sizeof(z));
+}
 
 cudaError_t noalloc_scratch_address(void **ptr)
 {

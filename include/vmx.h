@@ -282,6 +282,28 @@ int vmx_frames_noalloc(const void *ref, const void *dis, int width, int height,
 int vmx_checked_build(void);
 int vmx_check_status(void *stream);
 
+/*
+ * Timing builds (compiled with VMX_PHASE_TIMES=1, a profiling variant of the
+ * library; no counterpart in the pages): the frame kernel adds each phase's
+ * SM clock cycles, summed over its warps, and stamps a few events with the
+ * GPU's global nanosecond timer, into 16 counters on the current device that
+ * accumulate over launches:
+ *   [0] first warp's start (ns)      [1] last warp's end (ns)
+ *   [2] streaming items (cycles)     [3] look-back, waits included (cycles)
+ *   [4] plans and row runs (cycles)  [5] completion of items (cycles)
+ *   [6] last warp out of items (ns)  [7] first warp out of items (ns)
+ *   [8] walks, waits included (cycles) [9] last walk's end (ns)
+ *   [10] walks taken                 [11] items streamed
+ *   [12] longest walk (cycles)       [13] first walk's start (ns)
+ *   [14] row runs formed             [15] the SM clock rate (kHz)
+ * vmx_phase_times copies them into `out` (16 values, when not NULL), then
+ * clears them when `reset` is non-zero (the minima to all ones). It
+ * synchronises the device's default stream; call it with no launch of the
+ * library in flight. Errors: VMX_EINVAL in other builds or with neither an
+ * `out` nor `reset`, VMX_ECUDA.
+ */
+int vmx_phase_times(uint64_t *out, int reset);
+
 /* Name of a status code (and the last CUDA error for VMX_ECUDA). */
 const char *vmx_strerror(int status);
 

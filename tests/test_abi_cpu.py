@@ -35,10 +35,19 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_strerror(lib):
-    assert lib.vmx_version() == 10100
+    assert lib.vmx_version() == 10200
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert lib.vmx_strerror(code) and lib.vmx_strerror(code) != b"unknown status"
     assert lib.vmx_strerror(-99) == b"unknown status"
+
+
+def test_default_build_has_no_phase_times(lib):
+    """Only a timing build (VMX_PHASE_TIMES=1) keeps phase counters; the
+    default library refuses the call without touching the GPU."""
+    import numpy as np
+    out = np.zeros(16, dtype=np.uint64)
+    assert lib.vmx_phase_times(out.ctypes.data, 1) == _lib.VMX_EINVAL
+    assert lib.vmx_phase_times(None, 0) == _lib.VMX_EINVAL
 
 
 def test_default_build_is_not_checked(lib):
