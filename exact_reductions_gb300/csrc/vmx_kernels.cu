@@ -1944,6 +1944,20 @@ __global__ void __maxnreg__(FULL ? kMaxRegsFull : kMaxRegs) frames_kernel(Params
     // items, so the chunks would run one after another. Waits stay
     // deadlock-free: a warp works through its chunk in order, so the
     // smallest unfinished item is always some running warp's current item.
+    // The parameters as the functions the kernel calls without inlining see
+    // them: a copy in shared memory, so that no thread keeps a copy of its
+    // own in local memory for them to point at (the kernel reads its own).
+    // Measured per instance: the 16-bit aligned full-depth instance without
+    // the look-back runs about 1% faster with the per-thread copy (16 x
+    // 3840x2160: 98.6 against 99.7 us a call in a stream), every other one
+    // 1-5% faster with the shared copy.
+    constexpr bool kOwnCopy = sizeof(TS) == 2 && VEC && !FULL && !LOW;
+    __shared__ Params shared_params;
+    if (!kOwnCopy) {
+        if (threadIdx.x == 0) shared_params = p;
+        __syncthreads();
+    }
+    const Params &sp = kOwnCopy ? p : shared_params;
     __shared__ RowSlot item_rows[kWarps][kMaxRowsPerItem];  // sums of an item's rows
     __shared__ ParkSlot park[FULL && M ? kWarps : 1];         // an item waiting for its plan
     bool parked = false;
@@ -2064,7 +2078,7 @@ __global__ void __maxnreg__(FULL ? kMaxRegsFull : kMaxRegs) frames_kernel(Params
         // item parked meanwhile in the warp's shared slot): by then those
         // items are out, and the warp seldom waits.
         if (FULL && M) {
-            if (parked) resume_parked<VEC, FULL>(p, park[wid]);
+            if (parked) resume_parked<VEC, FULL>(sp, park[wid]);
             __syncwarp();
             if (lane < r1 - r0) {
                 park[wid].rows[0][lane] = my_r;
@@ -2082,9 +2096,9 @@ __global__ void __maxnreg__(FULL ? kMaxRegsFull : kMaxRegs) frames_kernel(Params
         }
 
         // C. completion.
-        complete_item<FULL>(p, f, j);
+        complete_item<FULL>(sp, f, j);
     }
-    if (FULL && M && parked) resume_parked<VEC, FULL>(p, park[wid]);
+    if (FULL && M && parked) resume_parked<VEC, FULL>(sp, park[wid]);
     pt_max(kPtOutLast, pt_now());
     pt_min(kPtOutFirst, pt_now());
 
@@ -2109,7 +2123,7 @@ __global__ void __maxnreg__(FULL ? kMaxRegsFull : kMaxRegs) frames_kernel(Params
         const int wf = wt / kParts, part = wt - wf * kParts;
         const long long tw = pt_clock();
         pt_min(kPtWalksStart, pt_now());
-        walk_part<TS, M, P, ODD, FULL, VEC>(p, wf, M ? part : 2);
+        walk_part<TS, M, P, ODD, FULL, VEC>(sp, wf, M ? part : 2);
         pt_cycles(kPtWalks, tw);
         pt_max(kPtWalkMax, (unsigned long long)(pt_clock() - tw));
         pt_add(kPtWalkTasks, 1ull);
