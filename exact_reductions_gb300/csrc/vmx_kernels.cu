@@ -2129,9 +2129,11 @@ __global__ void __maxnreg__(FULL ? kMaxRegsFull : kMaxRegs) frames_kernel(Params
         pt_add(kPtWalkTasks, 1ull);
         pt_max(kPtWalksEnd, pt_now());
     }
-    // Launched to overlap the previous kernel: finish after it, so that the
-    // stream's later work still follows both.
-    if (p.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Launched to overlap the previous kernel: the grid finishes after it, so
+    // that the stream's later work still follows both. One block waiting is
+    // enough for that; the others leave at once, and their slots go to the
+    // next calls (with small batches several calls run at a time).
+    if (p.overlap && blockIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
     pt_max(kPtEnd, pt_now());
 }
 

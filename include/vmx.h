@@ -145,13 +145,15 @@ int vmx_moment_psnr_frames(const void *ref, const void *dis, int width, int heig
  *   VMX_FLAG_OVERLAP  launch the kernel so that it may start while the
  *                     previous kernel on `stream` is still running
  *                     (programmatic dependent launch: its blocks take the SM
- *                     slots that kernel's blocks leave). The caller guarantees
- *                     that this call reads and writes nothing that kernel
- *                     writes (another workspace, other outputs) and that the
- *                     workspace was cleared beforehand (VMX_FLAG_CLEARED): a
- *                     clear enqueued between the two kernels would separate
- *                     them. The kernel does not finish before the previous
- *                     one, so later work on the stream follows both.
+ *                     slots that kernel's blocks leave; with small batches
+ *                     several calls run at a time). The caller guarantees
+ *                     that this call reads and writes nothing that an earlier
+ *                     kernel on `stream` still running may write (another
+ *                     workspace, other outputs) and that the workspace was
+ *                     cleared beforehand (VMX_FLAG_CLEARED): a clear enqueued
+ *                     between the two kernels would separate them. The kernel
+ *                     does not finish before the previous one, so later work
+ *                     on the stream follows both.
  * Both flags need a workspace. Errors as the other calls; unknown flags are
  * VMX_EINVAL. The pages have no counterpart: this is how a stream of batches
  * of one shape keeps the GPU busy between batches.
