@@ -238,6 +238,30 @@ def test_overlapped_batches_match_calls():
                 assert np.array_equal(u64(got[k]), u64(plain[k])), (i, k)
 
 
+def test_overlapped_look_back_batches_match_the_oracle():
+    """Four one-frame 7680x4320 batches (sums past 2^55: look-back, row runs,
+    walks) per replay, each kernel launched to overlap the one before, so
+    that several run at once: every batch's outputs equal the oracle's."""
+    wl = synth.WORKLOADS["C5c"]
+    ref, dis = wl.batch(4)
+    Rs = [to_device(ref[i:i + 1]) for i in range(4)]
+    Ds = [to_device(dis[i:i + 1]) for i in range(4)]
+    fg = api.FrameGraph(Rs[0], Ds[0], 16, s2_rows=True, sums=True, depth=4, refs=Rs, diss=Ds)
+    want = oracle_frames(ref, dis, 16, range(4))
+    for _ in range(2):
+        fg.replay()
+        torch.cuda.synchronize()
+        assert fg.status() == 0
+        for i in range(4):
+            got, w = fg.outs[i], want[i]
+            assert same_doubles(got["moments"].cpu().numpy()[0], w["moments"]), i
+            assert same_doubles(got["mse"].cpu().numpy()[0], w["mse"]), i
+            assert np.array_equal(u64(got["s2_rows"])[0], w["s2_rows"]), i
+            assert np.array_equal(u64(got["s2_sums"])[0], w["s2_sums"]), i
+            assert np.array_equal(u64(got["psnr_rows"])[0], w["psnr_rows"]), i
+            assert int(u64(got["noise_sums"])[0]) == w["noise_sum"], i
+
+
 def test_bounded_wait_gives_up_and_context_stays_usable(monkeypatch):
     """A walk that waits for a block count nothing reaches gives up after the
     poll limit, the call reports VMX_ETIMEOUT, and the next call is exact."""
