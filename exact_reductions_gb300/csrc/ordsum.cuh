@@ -240,7 +240,8 @@ VMX_HD Run lane_to_run(const LaneRun &r, uint64_t exact)
 }
 
 // The compact run of n terms under last place u = 2^sh, sh >= 1, while
-// n * 2u < 2^22 (the device forms 24-term runs in the same way).
+// n * 2u < 2^22 (the device runs each lane's stretch of a row, up to 1024
+// terms, the same way).
 //
 // Only t mod 2u matters for how a term rounds: writing t = 2u*m + v with
 // 0 <= v < 2u, the increment is 2u*m plus the rounded increment of v from the

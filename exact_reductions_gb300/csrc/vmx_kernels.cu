@@ -14,14 +14,16 @@
 //      pass 2^53 units, the number of odd terms per row. No float partials,
 //      no atomics on data.
 //   B. Only for frames above 2^23 pixels, whose sums can pass 2^55 units: the
-//      item's exact sums are published and the exact sum before the item is
-//      read by a decoupled look-back over the frame's earlier items (bounded
-//      wait). Rows planned in a binade from 55 up get their run (ADR-1497
-//      "Decision", third point) from passes of 32 lanes x 24 consecutive
-//      samples, re-reading the rows just streamed (mostly L2 hits).
-//   C. The item counts itself in its block (32 items) by a 32-bit
-//      acquire-release add; the block's last item to finish adds the block's
-//      item records into the block's record and marks it done. Warps that
+//      item's exact sums are published, and once the warp has streamed its
+//      next item the exact sum before the item is read by a decoupled
+//      look-back over the frame's earlier items (bounded wait). Rows planned
+//      in a binade from 55 up get their run (ADR-1497 "Decision", third
+//      point): the rows are asked into L2 and read again, each lane running
+//      one binary32 trajectory through a contiguous stretch of the row, the
+//      lanes' runs composed in order.
+//   C. The item counts itself in its block (32 items) by a 32-bit release
+//      add (acquire-release with B); the block's last item to finish adds the
+//      block's item records into the block's record and marks it done. Warps that
 //      find no item left take frames to walk: the crossing of 2^53 is found
 //      as soon as the blocks before it are complete, that row is walked term
 //      by term, and once the frame is complete each plane's later rows are
