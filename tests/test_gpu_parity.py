@@ -47,6 +47,16 @@ def test_single_feature_calls(features):
     run_and_check(ref, dis, 16, features=features)
 
 
+@pytest.mark.parametrize("features", [1, 2])
+def test_single_feature_calls_past_2_55(features):
+    """Moments alone on a frame past 2^55 (the look-back and the row runs
+    without psnr), and psnr alone on it (no look-back: only the moments
+    need one)."""
+    wl = synth.WORKLOADS["T2"]
+    ref, dis = wl.batch(1)
+    run_and_check(ref, dis, 16, features=features)
+
+
 def test_c5c_8k_batch_sampled():
     """64 frames of 16-bit 7680x4320 noise (four binade ranges): the full
     batch in one call, frames 0, 31 and 63 against the oracle."""
