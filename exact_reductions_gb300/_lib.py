@@ -39,6 +39,7 @@ SIGNATURES = {
     "vmx_moment_psnr_frames": (_i32, [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _vp, _vp, _vp, _vp,
                                       _vp, _vp, _vp, _sz, _vp]),
     "vmx_workspace_clear": (_i32, [_vp, _sz, _i32, _i32, _i32, _i32, _i32, _vp]),
+    "vmx_workspace_clear_n": (_i32, [_vp, _sz, _sz, _i32, _i32, _i32, _i32, _i32, _vp]),
     "vmx_integer_psnr_frames": (_i32, [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _vp, _vp, _vp,
                                        _vp]),
     "vmx_frames_ex": (_i32, [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,

@@ -124,9 +124,11 @@ class FrameGraph:
     graph, for a stream of batches of one shape.
 
     ``depth`` batches per replay, each with its own workspace and outputs
-    (``self.outs[i]``; ``self.out`` is the last): the workspaces are cleared
-    first, then the kernels run back to back, each launched to overlap the
-    one before it (``vmx_frames_ex`` with ``VMX_FLAG_OVERLAP``).
+    (``self.outs[i]``; ``self.out`` is the last): the workspaces (one
+    allocation) are cleared first by one strided set
+    (``vmx_workspace_clear_n``), then the kernels run back to back, each
+    launched to overlap the one before it (``vmx_frames_ex`` with
+    ``VMX_FLAG_OVERLAP``).
     ``refs``/``diss`` give each batch's input tensors (copy new frames into
     them between replays); by default every batch reads ``ref``/``dis``.
     Bounded device waits that give up are reported by ``status()``."""
@@ -147,7 +149,11 @@ class FrameGraph:
             raise ValueError("shape rejected by libvmx")
         m = bool(features & _lib.FEATURE_MOMENT)
         p = bool(features & _lib.FEATURE_PSNR)
-        self.ws = [workspace(need, dev) for _ in range(depth)]
+        # One allocation for the batches' workspaces, back to back, so that
+        # one strided clear (one graph node) readies them all.
+        self.ws_bytes = (need + _ALIGN - 1) // _ALIGN * _ALIGN
+        self.ws_all = workspace(self.ws_bytes * depth, dev)
+        self.ws = [self.ws_all[i * self.ws_bytes:(i + 1) * self.ws_bytes] for i in range(depth)]
         self.outs = []
         for _ in range(depth):
             o: Dict[str, torch.Tensor] = {}
@@ -167,9 +173,8 @@ class FrameGraph:
 
         def enqueue():
             st = _stream(dev)
-            for w in self.ws:
-                _lib.check(lib.vmx_workspace_clear(w.data_ptr(), w.numel(), W, H, bpc, F,
-                                                   features, st), "vmx workspace_clear")
+            _lib.check(lib.vmx_workspace_clear_n(self.ws_all.data_ptr(), self.ws_bytes, depth, W, H, bpc,
+                                                 F, features, st), "vmx workspace_clear_n")
             for i, ((r, d, _, _, _, _), o, w) in enumerate(zip(geo, self.outs, self.ws)):
                 flags = _lib.FLAG_CLEARED | (_lib.FLAG_OVERLAP if i else 0)
                 _lib.check(lib.vmx_frames_ex(

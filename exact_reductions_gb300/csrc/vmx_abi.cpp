@@ -363,6 +363,19 @@ int vmx_workspace_clear(void *workspace, size_t workspace_bytes, int width, int 
     return err == cudaSuccess ? VMX_OK : cuda_fail(err);
 }
 
+int vmx_workspace_clear_n(void *workspace, size_t workspace_bytes, size_t count, int width, int height,
+                          int bpc, int nframes, int features, void *stream)
+{
+    Layout L;
+    if (!workspace || count == 0 || !make_layout(width, height, bpc, nframes, features, &L)) return VMX_EINVAL;
+    if (workspace_bytes < L.total || workspace_bytes % 256 || (uintptr_t)workspace % 256) return VMX_EINVAL;
+    // One strided set covers every workspace's control words: one graph node.
+    const cudaError_t err =
+        cudaMemset2DAsync(static_cast<unsigned char *>(workspace) + L.off_ctrl, workspace_bytes, 0,
+                          L.ctrl_bytes, count, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? VMX_OK : cuda_fail(err);
+}
+
 int vmx_frames_ex(const void *ref, const void *dis, int width, int height, int64_t stride_bytes,
                   int bpc, int nframes, int features, double *moments, uint64_t *s2_rows,
                   uint64_t *s2_sums, uint64_t *psnr_rows, double *mse, uint64_t *noise_sums,

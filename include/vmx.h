@@ -162,6 +162,18 @@ int vmx_moment_psnr_frames(const void *ref, const void *dis, int width, int heig
 #define VMX_FLAG_OVERLAP 2u
 int vmx_workspace_clear(void *workspace, size_t workspace_bytes, int width, int height, int bpc,
                         int nframes, int features, void *stream);
+/*
+ * vmx_workspace_clear() of `count` workspaces laid out back to back in one
+ * allocation, workspace i at workspace + i * workspace_bytes, by one strided
+ * set on `stream` (one node when captured in a graph, where one clear per
+ * workspace would be `count`): the batches of one replay cleared at once.
+ * workspace_bytes a multiple of 256, at least vmx_workspace_bytes() for the
+ * shape; workspace 256-byte aligned. Errors: VMX_EINVAL (NULL, count 0,
+ * a shape the library rejects, sizes or alignment; nothing enqueued),
+ * VMX_ECUDA.
+ */
+int vmx_workspace_clear_n(void *workspace, size_t workspace_bytes, size_t count, int width, int height,
+                          int bpc, int nframes, int features, void *stream);
 int vmx_frames_ex(const void *ref, const void *dis, int width, int height, int64_t stride_bytes,
                   int bpc, int nframes, int features, double *moments, uint64_t *s2_rows,
                   uint64_t *s2_sums, uint64_t *psnr_rows, double *mse, uint64_t *noise_sums,

@@ -184,4 +184,13 @@ def test_pipelining_flags_are_checked_before_any_cuda_call():
                              _lib.FLAG_CLEARED, None) == _lib.VMX_EINVAL
     assert lib.vmx_workspace_clear(None, 1 << 20, 64, 8, 16, 1, 3, None) == _lib.VMX_EINVAL
     assert lib.vmx_workspace_clear(p, 16, 64, 8, 16, 1, 3, None) == _lib.VMX_EINVAL
+    # the clear of workspaces back to back: pointer, count, spacing (a
+    # multiple of 256, at least one workspace), shape
+    ok = 1 << 20
+    assert lib.vmx_workspace_clear_n(None, ok, 2, 64, 8, 16, 1, 3, None) == _lib.VMX_EINVAL
+    assert lib.vmx_workspace_clear_n(p, ok, 0, 64, 8, 16, 1, 3, None) == _lib.VMX_EINVAL
+    assert lib.vmx_workspace_clear_n(p, ok + 16, 2, 64, 8, 16, 1, 3, None) == _lib.VMX_EINVAL
+    assert lib.vmx_workspace_clear_n(p, 256, 2, 64, 8, 16, 1, 3, None) == _lib.VMX_EINVAL
+    assert lib.vmx_workspace_clear_n(ctypes.c_void_p(272), ok, 2, 64, 8, 16, 1, 3, None) == _lib.VMX_EINVAL
+    assert lib.vmx_workspace_clear_n(p, ok, 2, 64, 8, 7, 1, 3, None) == _lib.VMX_EINVAL
 
