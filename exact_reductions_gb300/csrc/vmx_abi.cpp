@@ -89,6 +89,12 @@ int bytes_per_sample(int bpc) { return bpc == 8 ? 1 : 2; }
 
 }  // namespace
 
+// Items a call has at least, rows allowing (shorter items for small calls).
+#ifndef VMX_FEW_ITEMS
+#define VMX_FEW_ITEMS 512
+#endif
+constexpr int kFewItems = VMX_FEW_ITEMS;
+
 bool make_layout(int width, int height, int bpc, int frames, int features, Layout *L)
 {
     if (width < 1 || width > 32768 || height < 1 || frames < 1 || bpc < 8 || bpc > 16)
@@ -102,7 +108,11 @@ bool make_layout(int width, int height, int bpc, int frames, int features, Layou
     L->ordered = m && bpc > 8 && n > ((int64_t)1 << 21);
     L->full = L->ordered && n > ((int64_t)1 << 23);
     const int target = L->full ? kItemPixelsFull : kItemPixels;
-    const int rpi = std::min(kMaxRowsPerItem, std::max(1, (target + width - 1) / width));
+    int rpi = std::min(kMaxRowsPerItem, std::max(1, (target + width - 1) / width));
+    // A call of very few items (a small frame or two) would leave most of
+    // the GPU idle and each warp walking its item's rows one after another:
+    // shorter items then, down to one row, until the call has kFewItems.
+    if (!L->full) rpi = (int)std::max<int64_t>(1, std::min<int64_t>(rpi, (int64_t)frames * height / kFewItems));
     const int ipf = (height + rpi - 1) / rpi;
     const int bpf = (ipf + kBlockItems - 1) / kBlockItems;
     if ((int64_t)frames * ipf >= (int64_t)INT_MAX / 2) return false;
