@@ -1944,8 +1944,10 @@ __global__ void __maxnreg__(FULL ? kMaxRegsFull : kMaxRegs) frames_kernel(Params
     // chunk is one item: an item's look-back waits for the item before it,
     // and in a longer chunk that item would wait for its owner's earlier
     // items, so the chunks would run one after another. Waits stay
-    // deadlock-free: a warp works through its chunk in order, so the
-    // smallest unfinished item is always some running warp's current item.
+    // deadlock-free: streaming an item never waits, and a look-back (taken
+    // up for a parked item once the warp has streamed its next one) waits
+    // only for earlier items to have streamed, each of which a running warp
+    // holds or has finished.
     // The parameters as the functions the kernel calls without inlining see
     // them: a copy in shared memory, so that no thread keeps a copy of its
     // own in local memory for them to point at (the kernel reads its own).
